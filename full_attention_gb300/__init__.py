@@ -1,0 +1,187 @@
+"""Python binding of the GB300 paged-KV attention library.
+
+Argument marshalling only: every step of the store, decode and extend paths
+runs in the CUDA kernels of ``libfa_gb300.so`` behind the C ABI declared in
+``include/fa.h``.  PyTorch supplies device memory and streams.  Importing this
+package raises if the library has not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FULL, SLIDING = 0, 1
+KV_BF16, KV_INT8 = 0, 1
+KV_OWN, KV_AUTO = -1, -2
+DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT = 1, 2, 4, 8
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NOT_BOUND, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4, 5
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("window", ctypes.c_int32), ("kv_source", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float)]
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_lib.fa_status_string(status).decode()}: {msg}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with full_attention_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    sig = {
+        "fa_cache_create": (i32, [ctypes.POINTER(LayerDesc), i32, i32, i32, i32, ctypes.POINTER(vp)]),
+        "fa_cache_destroy": (None, [vp]),
+        "fa_cache_layer_source": (i32, [vp, i32, ctypes.POINTER(i32)]),
+        "fa_cache_slab_bytes": (i32, [vp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+        "fa_cache_bind_slab": (i32, [vp, i32, vp, vp, vp, vp]),
+        "fa_kv_bytes_per_token": (sz, [vp, i32]),
+        "fa_kv_store": (i32, [vp, i32, vp, vp, vp, i32, vp]),
+        "fa_decode_workspace_bytes": (sz, [vp, i32, i32, i32]),
+        "fa_paged_decode_attn": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
+        "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
+        "fa_get_device_error": (i32, [ctypes.POINTER(i32), vp]),
+        "fa_last_error": (ctypes.c_char_p, []),
+        "fa_status_string": (ctypes.c_char_p, [i32]),
+        "fa_version": (i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise FAError(status, _lib.fa_last_error().decode())
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _desc(d: dict) -> LayerDesc:
+    return LayerDesc(int(d["kind"]), int(d["head_dim"]), int(d["num_q_heads"]), int(d["num_kv_heads"]),
+                     int(d.get("window", 0)), int(d.get("kv_source", KV_OWN)), float(d["sm_scale"]))
+
+
+class Cache:
+    """Host descriptor of a paged KV cache: the layer -> slab map over one page pool.
+
+    `layers` is a list of dicts with the fa_layer_desc fields.  Bound slab
+    tensors are referenced here so they outlive the descriptor's use.
+    """
+
+    def __init__(self, layers, num_pages: int, page_size: int, kv_dtype: int = KV_BF16):
+        self.layers = [dict(d) for d in layers]
+        self.num_pages, self.page_size, self.kv_dtype = int(num_pages), int(page_size), int(kv_dtype)
+        arr = (LayerDesc * len(layers))(*[_desc(d) for d in layers])
+        h = ctypes.c_void_p()
+        _check(_lib.fa_cache_create(arr, len(layers), self.num_pages, self.page_size, self.kv_dtype,
+                                    ctypes.byref(h)))
+        self._h = h
+        self._slabs = {}
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.fa_cache_destroy(h)
+            self._h = None
+
+    def source(self, layer: int) -> int:
+        out = ctypes.c_int32()
+        _check(_lib.fa_cache_layer_source(self._h, layer, ctypes.byref(out)))
+        return out.value
+
+    def slab_bytes(self, layer: int):
+        kv, sc = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(_lib.fa_cache_slab_bytes(self._h, layer, ctypes.byref(kv), ctypes.byref(sc)))
+        return kv.value, sc.value
+
+    def bytes_per_token(self, kind: int) -> int:
+        return int(_lib.fa_kv_bytes_per_token(self._h, kind))
+
+    def bind(self, layer: int, k, v, k_scale=None, v_scale=None) -> None:
+        _check(_lib.fa_cache_bind_slab(self._h, layer, _p(k), _p(v), _p(k_scale), _p(v_scale)))
+        self._slabs[layer] = (k, v, k_scale, v_scale)
+
+    def allocate(self, device="cuda") -> dict:
+        """Allocate (torch) and bind a slab for every owning layer; returns
+        {layer: (k, v, k_scale, v_scale)} with k, v shaped [num_pages][Hkv][page_size][D]."""
+        out = {}
+        for i, d in enumerate(self.layers):
+            if self.source(i) != i:
+                continue
+            shape = (self.num_pages, d["num_kv_heads"], self.page_size, d["head_dim"])
+            dt = torch.int8 if self.kv_dtype == KV_INT8 else torch.bfloat16
+            k = torch.empty(shape, dtype=dt, device=device)
+            v = torch.empty(shape, dtype=dt, device=device)
+            ks = vs = None
+            if self.kv_dtype == KV_INT8:
+                ks = torch.empty(shape[:3], dtype=torch.float32, device=device)
+                vs = torch.empty(shape[:3], dtype=torch.float32, device=device)
+            self.bind(i, k, v, ks, vs)
+            out[i] = (k, v, ks, vs)
+        return out
+
+    def slab(self, layer: int):
+        """(k, v, k_scale, v_scale) tensors the layer reads (its source's for a shared layer)."""
+        return self._slabs[self.source(layer)]
+
+    def store(self, layer: int, k, v, slot_mapping, stream=None) -> None:
+        _check(_lib.fa_kv_store(self._h, layer, _p(k), _p(v), _p(slot_mapping), int(slot_mapping.numel()),
+                                _s(stream)))
+
+    def decode_workspace_bytes(self, layer: int, batch: int, max_seq_len: int) -> int:
+        return int(_lib.fa_decode_workspace_bytes(self._h, layer, batch, max_seq_len))
+
+    def decode(self, layer: int, q, block_table, seq_lens, max_seq_len: int, out, lse=None, workspace=None,
+               stream=None) -> None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(_lib.fa_paged_decode_attn(self._h, layer, _p(q), _p(block_table), int(block_table.shape[1]),
+                                         _p(seq_lens), int(q.shape[0]), int(max_seq_len), _p(out), _p(lse),
+                                         _p(workspace), ws_bytes, _s(stream)))
+
+    def extend(self, layer: int, q, k_ext, v_ext, qo_indptr, prefix_lens, block_table, max_q_len: int,
+               max_prefix_len: int, out, lse=None, stream=None) -> None:
+        maxp = int(block_table.shape[1]) if block_table is not None else 0
+        _check(_lib.fa_paged_extend_attn(self._h, layer, _p(q), _p(k_ext), _p(v_ext), _p(qo_indptr),
+                                         _p(prefix_lens), _p(block_table), maxp, int(prefix_lens.numel()),
+                                         int(max_q_len), int(max_prefix_len), _p(out), _p(lse), _s(stream)))
+
+
+def device_error(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device error word (FA_DEV_ERR_* bits)."""
+    code = ctypes.c_int32()
+    _check(_lib.fa_get_device_error(ctypes.byref(code), _s(stream)))
+    return code.value
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A 256-byte-aligned scratch buffer of at least nbytes (torch-allocated)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)

@@ -1,0 +1,131 @@
+// Internal declarations shared by the host API and the kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "fa.h"
+
+namespace fa {
+
+// Token rows are processed in 16-row tiles: one m16 tile of the warp MMAs and
+// one TMA box height.  Page sizes are multiples of it.
+constexpr int kTile = 16;
+
+struct Slab {
+  void* k = nullptr;
+  void* v = nullptr;
+  float* k_scale = nullptr;
+  float* v_scale = nullptr;
+  bool bound = false;
+  // TMA descriptors over K and V, 3-D: (64-element column block, block index,
+  // row) with rows = num_pages * Hkv * page_size; see fa_cache_bind_slab.
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  // int8 format: 2-D maps over the fp32 scales, one 16-float box per tile.
+  CUtensorMap tm_ks;
+  CUtensorMap tm_vs;
+};
+
+struct Layer {
+  fa_layer_desc d;
+  int owner = -1;   // slab owner (itself if it owns a slab)
+};
+
+}  // namespace fa
+
+struct fa_cache {
+  std::vector<fa::Layer> layers;
+  std::vector<fa::Slab> slabs;   // indexed by layer; only owners are bound
+  int32_t num_pages = 0;
+  int32_t page_size = 0;
+  int32_t kv_dtype = FA_KV_BF16;
+};
+
+namespace fa {
+
+// thread-local error message
+fa_status fail(fa_status st, const char* fmt, ...);
+
+// Device error word (one per device, file-scope __device__ storage).
+unsigned int* device_error_word(cudaError_t* err);
+
+int sm_count();
+
+// Set a kernel's dynamic shared-memory limit once per device.
+cudaError_t set_smem_once(const void* fn, int bytes, unsigned int* done_mask);
+
+// ---------------------------------------------------------------- decode plan
+struct DecodePlan {
+  int head_chunks = 1;      // ceil(g / 8): query heads are packed 8 per MMA column block
+  int max_tiles = 0;        // 16-row tiles a sequence can touch under the bound
+  int tiles_per_split = 0;  // tiles one CTA walks
+  int splits = 0;           // CTAs per (sequence, KV head, head chunk)
+  size_t o_bytes = 0;       // partial outputs: float [B][Hq][splits][D]
+  size_t ml_bytes = 0;      // partial (max, sum): float [B][Hq][splits][2]
+  size_t ws_bytes = 0;
+};
+DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len);
+
+struct StoreArgs {
+  const void* k;
+  const void* v;
+  const int32_t* slots;
+  void* k_slab;
+  void* v_slab;
+  float* k_scale;
+  float* v_scale;
+  int T, Hkv, D, page_size, num_pages, kv_dtype;
+  unsigned int* err;
+};
+cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const float* k_scale;
+  const float* v_scale;
+  void* out;
+  float* lse;
+  float* o_part;
+  float* ml_part;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_ks;
+  const CUtensorMap* tm_vs;
+  int B, Hq, Hkv, D, kind, window, page_size, num_pages, max_pages_per_seq, max_seq_len, kv_dtype;
+  float sm_scale;
+  DecodePlan plan;
+  unsigned int* err;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+struct ExtendArgs {
+  const void* q;
+  const void* k_ext;
+  const void* v_ext;
+  const int32_t* qo_indptr;
+  const int32_t* prefix_lens;
+  const int32_t* block_table;
+  const void* k_slab;
+  const void* v_slab;
+  const float* k_scale;
+  const float* v_scale;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_ks;
+  const CUtensorMap* tm_vs;
+  void* out;
+  float* lse;
+  int B, Hq, Hkv, D, kind, window, page_size, num_pages, max_pages_per_seq, max_q_len,
+      max_prefix_len, kv_dtype;
+  float sm_scale;
+  unsigned int* err;
+};
+cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s);
+
+}  // namespace fa

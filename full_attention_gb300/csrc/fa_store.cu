@@ -1,0 +1,156 @@
+// Paged KV store: scatter post-RoPE k, v rows of new tokens into their slots
+// ("FreeToken PR #898", description bullet on store_kv; "unsloth commit
+// dee9371": the store layer writes its post-rotary k, v into its paged cache).
+//
+// One warp moves one (token, KV head, K-or-V) row with 16-byte vector loads
+// and stores.  The int8 per-token-head format quantises the row on the way:
+// a = max|x| (fp32, warp-shuffle reduction), s = a / 127, c = rint(x / s)
+// clamped to [-127, 127], both divisions IEEE round-to-nearest.
+#include <cstdio>
+#include <mutex>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+// Device error word: FA_DEV_ERR_* bits OR-ed in by every kernel of the library.
+__device__ unsigned int g_fa_device_error;
+
+namespace fa {
+
+unsigned int* device_error_word(cudaError_t* err) {
+  static std::mutex mu;
+  static unsigned int* ptrs[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fa_device_error);
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  *err = cudaSuccess;
+  return ptrs[dev];
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rows = a.T * a.Hkv * 2;
+  if (warp >= rows) return;
+  const int which = warp & 1;            // 0: K, 1: V
+  const int th = warp >> 1;
+  const int t = th / a.Hkv, h = th % a.Hkv;
+  const int slot = __ldg(a.slots + t);
+  if (slot < 0) return;                  // padding token
+  const int page = slot / a.page_size, off = slot % a.page_size;
+  if (page >= a.num_pages) {
+    if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(which ? a.v : a.k) +
+                                                    (static_cast<size_t>(t) * a.Hkv + h) * D);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) +
+                                        ((static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off) * D);
+#pragma unroll
+  for (int i = 0; i < D / 256; ++i) dst[i * 32 + lane] = __ldg(src + i * 32 + lane);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&x)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
+  constexpr int NV = D / 256;            // 16-byte vectors (8 values) per lane
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rows = a.T * a.Hkv * 2;
+  if (warp >= rows) return;
+  const int which = warp & 1;
+  const int th = warp >> 1;
+  const int t = th / a.Hkv, h = th % a.Hkv;
+  const int slot = __ldg(a.slots + t);
+  if (slot < 0) return;
+  const int page = slot / a.page_size, off = slot % a.page_size;
+  if (page >= a.num_pages) {
+    if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(which ? a.v : a.k) +
+                                                    (static_cast<size_t>(t) * a.Hkv + h) * D);
+  float x[NV][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    bf16x8_to_f32(__ldg(src + i * 32 + lane), x[i]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = __fdiv_rn(amax, 127.0f);
+  const size_t row = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
+  int8_t* dst = static_cast<int8_t*>(which ? a.v_slab : a.k_slab) + row * D;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      int c = 0;
+      if (amax != 0.0f) {
+        float qv = rintf(__fdiv_rn(x[i][e], s));
+        qv = fminf(fmaxf(qv, -127.0f), 127.0f);
+        c = static_cast<int>(qv);
+      }
+      packed[e >> 2] |= (static_cast<uint32_t>(c) & 0xffu) << (8 * (e & 3));
+    }
+    *reinterpret_cast<uint2*>(dst + i * 256 + lane * 8) = make_uint2(packed[0], packed[1]);
+  }
+  if (lane == 0) (which ? a.v_scale : a.k_scale)[row] = s;
+}
+
+cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {
+  const long warps = static_cast<long>(a.T) * a.Hkv * 2;
+  const int block = 256;
+  const long grid = (warps * 32 + block - 1) / block;
+  if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
+  if (a.kv_dtype == FA_KV_INT8) {
+    if (a.D == 256) store_int8_kernel<256><<<grid, block, 0, s>>>(a);
+    else store_int8_kernel<512><<<grid, block, 0, s>>>(a);
+  } else {
+    if (a.D == 256) store_bf16_kernel<256><<<grid, block, 0, s>>>(a);
+    else store_bf16_kernel<512><<<grid, block, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+extern "C" fa_status fa_get_device_error(int32_t* code, void* stream) {
+  if (!code) return fa::fail(FA_ERR_INVALID_ARG, "code is NULL");
+  cudaError_t ce;
+  unsigned int* p = fa::device_error_word(&ce);
+  if (!p) return fa::fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if ((ce = cudaStreamSynchronize(s)) != cudaSuccess ||
+      (ce = cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      (ce = cudaMemsetAsync(p, 0, sizeof(v), s)) != cudaSuccess || (ce = cudaStreamSynchronize(s)) != cudaSuccess)
+    return fa::fail(FA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(ce));
+  *code = static_cast<int32_t>(v);
+  return FA_OK;
+}

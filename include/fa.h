@@ -1,0 +1,236 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * Gemma-4-style attention over a block-table KV cache with two per-layer
+ * regimes and KV sharing:
+ *
+ *   full layers     purely causal, kv_pos <= q_pos, head_dim 512;
+ *   sliding layers  causal and q_pos - kv_pos < W, head_dim 256, where W
+ *                   counts the current token (W = 1024 sees 1023 earlier
+ *                   positions; a FlashInfer-style inclusive window_left is
+ *                   W - 1).
+ *                   ["unsloth gemma4_flex_inference.py" commit history,
+ *                    commit "block mask per attention regime";
+ *                    "pegainfer issue #807", Description, second paragraph]
+ *
+ *   KV-shared layers own no slab: they read the slab (and, in the int8
+ *   format, the scales) of their source, the last earlier owning layer of the
+ *   same attention type, and the store skips them.
+ *                   ["FreeToken PR #898: read the source layer's kv slab on
+ *                    kv-shared layers", description bullets;
+ *                    "unsloth commit dee9371", commit message]
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Ownership.  The caller allocates and owns every device buffer (slabs,
+ *   scales, q/k/v, tables, outputs, workspace) and every stream.  The library
+ *   owns only the host-side descriptor returned by fa_cache_create.  No call
+ *   allocates or frees device memory.
+ * - Streams.  `stream` is a cudaStream_t handle passed as void*; NULL is the
+ *   legacy default stream.  Device work is enqueued asynchronously; a call
+ *   returns after host-side validation and the launches.
+ * - Errors.  Every call returns an fa_status.  Host-side validation failures
+ *   return without launching anything; fa_last_error() gives a message
+ *   (thread-local).  Launch failures return FA_ERR_CUDA.  Faults that only the
+ *   device can see (a page id outside [0, num_pages), a slot outside the pool,
+ *   a sequence longer than the bound the caller promised, a bounded wait that
+ *   ran out) never trap: the kernel skips the access, sets a bit in a device
+ *   error word and finishes; fa_get_device_error() reads and clears it.
+ * - Types.  bf16 tensors are IEEE bfloat16 (2 bytes); int32 tables are
+ *   little-endian int32_t; all tensors are dense row-major with the shapes
+ *   given below.  Device pointers must be 16-byte aligned.
+ * - GQA.  Query head j reads KV head j / (Hq / Hkv); Hq must be a multiple of
+ *   Hkv.  (The pages do not state the mapping; contiguous groups are the
+ *   usual repeat-kv convention.)
+ *
+ * Physical layouts (chosen by this library; results depend only on the
+ * logical rows, so any physical page order gives the same attention output):
+ *   bf16 slab     K, V: bf16 [num_pages][Hkv][page_size][D]
+ *   int8 slab     K, V: int8 [num_pages][Hkv][page_size][D]  (codes)
+ *                 k_scale, v_scale: float [num_pages][Hkv][page_size]
+ *   slot          page * page_size + offset; logical position p of sequence b
+ *                 lives in page block_table[b][p / page_size], offset
+ *                 p % page_size.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(FA_BUILD) && defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer ... */
+  FA_ERR_UNSUPPORTED = 2,   /* a layout the method refuses or this build lacks */
+  FA_ERR_NOT_BOUND = 3,     /* the layer's slab owner has no slab bound yet   */
+  FA_ERR_WORKSPACE = 4,     /* workspace smaller than fa_decode_workspace_bytes */
+  FA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed           */
+  FA_ERR_DEVICE = 6         /* reserved for device-side error reports         */
+} fa_status;
+
+typedef enum { FA_KV_BF16 = 0, FA_KV_INT8 = 1 } fa_kv_dtype;
+typedef enum { FA_FULL = 0, FA_SLIDING = 1 } fa_layer_kind;
+
+/* kv_source values besides an explicit earlier layer index */
+#define FA_KV_OWN (-1)    /* the layer owns a slab */
+#define FA_KV_AUTO (-2)   /* shared: source = last earlier owning layer of its kind */
+
+/* Device error bits reported by fa_get_device_error */
+#define FA_DEV_ERR_PAGE 0x1u       /* a visible page id was outside [0, num_pages) */
+#define FA_DEV_ERR_SLOT 0x2u       /* a store slot was >= num_pages * page_size    */
+#define FA_DEV_ERR_BOUND 0x4u      /* a length exceeded the caller's max bound      */
+#define FA_DEV_ERR_TIMEOUT 0x8u    /* a bounded barrier wait ran out                */
+
+/* One attention layer.  kind: fa_layer_kind.  head_dim: 256 or 512 (other
+ * widths return FA_ERR_UNSUPPORTED; the pages name exactly these two).
+ * window: Gemma's W for sliding layers (>= 1, counts the current token);
+ * ignored for full layers.  kv_source: FA_KV_OWN, FA_KV_AUTO, or an explicit
+ * earlier owning layer of the same kind and KV geometry.  sm_scale: the
+ * softmax scale applied to q.k (usually 1/sqrt(head_dim)). */
+typedef struct {
+  int32_t kind;
+  int32_t head_dim;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t window;
+  int32_t kv_source;
+  float sm_scale;
+} fa_layer_desc;
+
+typedef struct fa_cache fa_cache;   /* opaque host-side descriptor */
+
+/* Build the layer -> slab map for n_layers layers sharing one page pool of
+ * num_pages pages of page_size tokens, in kv_dtype.  Resolves every shared
+ * layer's source by the rule of "FreeToken PR #898" (description, first
+ * bullet: the last earlier layer of its attention type) and refuses, with
+ * FA_ERR_UNSUPPORTED, a shared layer that has no earlier owning layer of its
+ * kind, a source that is itself shared or of another kind, or a source whose
+ * head_dim / num_kv_heads differ (review thread of the same PR: such a
+ * layout is refused, not served).  page_size must be a multiple of 16 and at
+ * most 256.  On success *out receives a descriptor to free with
+ * fa_cache_destroy.  Host only; no CUDA call. */
+FA_API fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t num_pages,
+                          int32_t page_size, int32_t kv_dtype, fa_cache** out);
+
+/* Free the descriptor (NULL is accepted).  Device buffers stay the caller's. */
+FA_API void fa_cache_destroy(fa_cache* cache);
+
+/* Slab owner of `layer`: the layer itself if it owns a slab, else its
+ * resolved source.  Host only. */
+FA_API fa_status fa_cache_layer_source(const fa_cache* cache, int32_t layer, int32_t* slab_owner);
+
+/* Bytes the caller must allocate for one of K or V of an owning layer
+ * (num_pages * Hkv * page_size * D * elem) and for one of k_scale or v_scale
+ * (0 in bf16).  A shared layer reports 0 and 0.  Host only. */
+FA_API fa_status fa_cache_slab_bytes(const fa_cache* cache, int32_t layer, size_t* kv_bytes,
+                              size_t* scale_bytes);
+
+/* Bind caller-owned device buffers as the slab of an owning layer (k, v in the
+ * layout above; k_scale, v_scale required in the int8 format, ignored in
+ * bf16).  Binding a shared layer returns FA_ERR_INVALID_ARG: it reads its
+ * source's slab.  Rebinding replaces the previous pointers.  Encodes the TMA
+ * descriptors the kernels use, so it needs a CUDA device (FA_ERR_CUDA when the
+ * driver cannot be reached). */
+FA_API fa_status fa_cache_bind_slab(fa_cache* cache, int32_t layer, void* k, void* v, float* k_scale,
+                             float* v_scale);
+
+/* Bytes one token costs across the slabs of the owning layers of `kind`
+ * (fa_layer_kind): per owning layer and KV head 2 * (D * elem + scale bytes).
+ * Shared layers cost nothing ("FreeToken PR #898", description bullet on
+ * kv_cache_group_specs; its "End to end" section prints these unit_bytes).
+ * Host only. */
+FA_API size_t fa_kv_bytes_per_token(const fa_cache* cache, int32_t kind);
+
+/* Paged KV store ("FreeToken PR #898", description bullet on HybridSWAKVCache
+ * and store_kv; "unsloth commit dee9371": the store layer writes its
+ * post-rotary k, v into its paged cache).
+ * k, v: bf16 [T][Hkv][D] post-RoPE rows of T new tokens (device).
+ * slot_mapping: int32 [T] (device); token t goes to slot slot_mapping[t];
+ * a negative slot is padding and is skipped; a slot >= num_pages * page_size
+ * is skipped and sets FA_DEV_ERR_SLOT.
+ * bf16 format: a bit-exact copy.  int8 format: per (token, head), separately
+ * for K and V, a = max|x| in fp32, s = a / 127 (IEEE division), codes
+ * c = clamp(rint(x / s), -127, 127) with rint rounding half to even; a = 0
+ * gives s = 0 and all-zero codes.
+ * A KV-shared layer stores nothing: FA_OK, no launch.  T == 0: FA_OK, no
+ * launch. */
+FA_API fa_status fa_kv_store(fa_cache* cache, int32_t layer, const void* k, const void* v,
+                      const int32_t* slot_mapping, int32_t T, void* stream);
+
+/* Workspace bytes fa_paged_decode_attn needs for this layer, batch and bound
+ * on the sequence lengths (the split-K partial results).  Host only. */
+FA_API size_t fa_decode_workspace_bytes(const fa_cache* cache, int32_t layer, int32_t B,
+                                 int32_t max_seq_len);
+
+/* Paged decode attention, one new token per sequence (split-K online softmax,
+ * GQA-packed so each KV page is read once for all Hq / Hkv query heads).
+ * q: bf16 [B][Hq][D] (device).  block_table: int32 [B][max_pages_per_seq].
+ * seq_lens: int32 [B], the context length INCLUDING the current token, whose
+ * k, v must already be stored; the query sits at q_pos = seq_lens[b] - 1.
+ * Full layers attend to positions [0, q_pos]; sliding layers to
+ * [max(0, q_pos - W + 1), q_pos] and read only the pages that hold them, so
+ * block-table entries outside the window may be -1 (never read).
+ * A shared layer reads its source's slab and scales.
+ * max_seq_len: host bound on every seq_lens[b] (longer ones set
+ * FA_DEV_ERR_BOUND and are cut at the bound).
+ * out: bf16 [B][Hq][D].  lse: optional float [B][Hq], natural-log
+ * sum-exp of the scaled scores.  seq_lens[b] <= 0 gives out = 0 and
+ * lse = -inf.  workspace: device scratch of at least
+ * fa_decode_workspace_bytes(cache, layer, B, max_seq_len) bytes (may be NULL
+ * when that is 0).  Reference: "unsloth commit dee9371" (shared layers read
+ * the source's paged cache on decode) and the regimes above. */
+FA_API fa_status fa_paged_decode_attn(fa_cache* cache, int32_t layer, const void* q,
+                               const int32_t* block_table, int32_t max_pages_per_seq,
+                               const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Chunked-prefill / extend attention ("FreeToken PR #898", description: the
+ * extend kernel takes the prefix from the slab and the current chunk from
+ * k_extend / v_extend; "pegainfer issue #807": the prefill chunk size is a
+ * capacity parameter).  Sequence b has prefix_lens[b] = P_b tokens already
+ * in the cache and n_b = qo_indptr[b+1] - qo_indptr[b] new tokens; new token
+ * i sits at position P_b + i and attends to prefix positions (from the slab,
+ * dequantised in int8) and chunk positions P_b + j, j <= i (from k_ext /
+ * v_ext, bf16, never quantised), under the layer's mask.
+ * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
+ * (for a shared layer: the source layer's current k, v).  qo_indptr: int32
+ * [B+1], non-decreasing, qo_indptr[0] = 0.  prefix_lens: int32 [B].
+ * max_q_len >= every n_b, max_prefix_len >= every P_b (longer ones set
+ * FA_DEV_ERR_BOUND and are cut).  out: bf16 [N][Hq][D]; lse: optional float
+ * [N][Hq].  The chunk's own k, v are read from k_ext / v_ext even if they
+ * were stored first. */
+FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void* q, const void* k_ext,
+                               const void* v_ext, const int32_t* qo_indptr,
+                               const int32_t* prefix_lens, const int32_t* block_table,
+                               int32_t max_pages_per_seq, int32_t B, int32_t max_q_len,
+                               int32_t max_prefix_len, void* out, float* lse, void* stream);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device (FA_DEV_ERR_* bits; 0 = no error). */
+FA_API fa_status fa_get_device_error(int32_t* code, void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+FA_API const char* fa_last_error(void);
+
+/* Name of a status code. */
+FA_API const char* fa_status_string(int32_t status);
+
+/* Library ABI version (major * 100 + minor). */
+FA_API int32_t fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

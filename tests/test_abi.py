@@ -1,0 +1,141 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+function include/fa.h declares, and its host-side logic (layer -> slab map,
+source rule, refusals, bytes per token, workspace sizing) agrees with the
+oracle and with the numbers the pages print."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import FULL, SLIDING, KV_AUTO, KV_OWN
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import full_attention_gb300 as fa
+    return fa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["fa_cache_create", "fa_cache_destroy", "fa_cache_bind_slab", "fa_cache_layer_source",
+                     "fa_kv_bytes_per_token", "fa_kv_store", "fa_decode_workspace_bytes",
+                     "fa_paged_decode_attn", "fa_paged_extend_attn", "fa_get_device_error", "fa_last_error"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = ctypes.CDLL(fa.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert fa.lib().fa_version() >= 100
+
+
+def lay(kind, D, hq, hkv, W=0, src=KV_OWN):
+    return dict(kind=kind, head_dim=D, num_q_heads=hq, num_kv_heads=hkv, window=W if kind == SLIDING else 0,
+                kv_source=src, sm_scale=float(np.float32(1 / np.sqrt(D))))
+
+
+def e_series(n_layers, period, n_owning, hkv, share=True):
+    out = []
+    for i in range(n_layers):
+        full = (i % period) == period - 1
+        src = KV_OWN if (i < n_owning or not share) else KV_AUTO
+        out.append(lay(FULL if full else SLIDING, 512 if full else 256, 8, hkv, 512, src))
+    return out
+
+
+@pytest.mark.parametrize("model", [(35, 5, 15, 1), (42, 6, 24, 2)], ids=["E2B", "E4B"])
+def test_sources_and_bytes_match_oracle(fa, model):
+    for share in (True, False):
+        layers = e_series(*model, share=share)
+        for dtype in (fa.KV_BF16, fa.KV_INT8):
+            c = fa.Cache(layers, 64, 16, dtype)
+            want = oracle.resolve_kv_sources(layers)
+            got = [c.source(i) for i in range(len(layers))]
+            assert got == [i if s == -1 else s for i, s in enumerate(want)]
+            for kind in (FULL, SLIDING):
+                assert c.bytes_per_token(kind) == oracle.kv_bytes_per_token(layers, kind, dtype)
+            for i in range(len(layers)):
+                kv, sc = c.slab_bytes(i)
+                if want[i] == -1:
+                    elem = 1 if dtype == fa.KV_INT8 else 2
+                    assert kv == 64 * layers[i]["num_kv_heads"] * 16 * layers[i]["head_dim"] * elem
+                    assert sc == (64 * layers[i]["num_kv_heads"] * 16 * 4 if dtype == fa.KV_INT8 else 0)
+                else:
+                    assert (kv, sc) == (0, 0)
+
+
+def test_bytes_per_token_golden(fa):
+    """The unit_bytes the "FreeToken PR #898" End-to-end section prints."""
+    rows = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", "kv_bytes_per_token.txt"))
+            if l.strip() and not l.startswith("#")]
+    models = {"E2B": (35, 5, 15, 1), "E4B": (42, 6, 24, 2)}
+    for model, f, sharing, full, window in rows:
+        c = fa.Cache(e_series(*models[model], share=sharing == "after"), 8, 16,
+                     fa.KV_INT8 if f == "int8" else fa.KV_BF16)
+        assert (c.bytes_per_token(FULL), c.bytes_per_token(SLIDING)) == (int(full), int(window))
+
+
+def test_refusals(fa):
+    bad_layouts = [
+        [lay(FULL, 512, 8, 1), lay(SLIDING, 256, 8, 1, 512, KV_AUTO)],           # no earlier sliding owner
+        [lay(FULL, 512, 8, 1), lay(FULL, 512, 8, 1, 0, KV_AUTO), lay(FULL, 512, 8, 1, 0, 1)],  # shared source
+        [lay(FULL, 512, 8, 1), lay(FULL, 512, 8, 2, 0, KV_AUTO)],                # geometry differs
+        [lay(SLIDING, 256, 8, 1, 512), lay(FULL, 512, 8, 1, 0, 0)],              # source of another kind
+        [lay(FULL, 128, 8, 1)],                                                  # head_dim not instantiated
+    ]
+    for layers in bad_layouts:
+        with pytest.raises(fa.FAError) as e:
+            fa.Cache(layers, 8, 16)
+        assert e.value.status == fa.ERR_UNSUPPORTED
+    for layers, st in [([lay(SLIDING, 256, 8, 1, 0)], fa.ERR_INVALID_ARG),      # W < 1
+                       ([lay(FULL, 512, 6, 4)], fa.ERR_INVALID_ARG)]:            # Hq not a multiple of Hkv
+        with pytest.raises(fa.FAError) as e:
+            fa.Cache(layers, 8, 16)
+        assert e.value.status == st
+    for ps in (8, 24, 512):
+        with pytest.raises(fa.FAError) as e:
+            fa.Cache([lay(FULL, 512, 8, 1)], 8, ps)
+        assert e.value.status == fa.ERR_UNSUPPORTED
+
+
+def test_unbound_and_shared_bind_errors(fa):
+    c = fa.Cache([lay(SLIDING, 256, 8, 1, 64), lay(SLIDING, 256, 8, 1, 64, KV_AUTO)], 8, 16)
+    # a shared layer cannot be bound; its source's slab is the one it reads
+    with pytest.raises(fa.FAError) as e:
+        c.bind(1, None, None)
+    assert e.value.status == fa.ERR_INVALID_ARG
+    # the store on a shared layer is a no-op that needs nothing bound
+    st = fa.lib().fa_kv_store(c._h, 1, None, None, None, 4, None)
+    assert st == fa.OK
+    # the owner has no slab yet
+    st = fa.lib().fa_kv_store(c._h, 0, None, None, None, 4, None)
+    assert st == fa.ERR_NOT_BOUND
+
+
+def test_decode_workspace_sizing(fa):
+    for D, kind, W in [(512, FULL, 0), (256, SLIDING, 512), (256, SLIDING, 1024)]:
+        c = fa.Cache([lay(kind, D, 8, 1, W)], 1024, 16)
+        for B, maxlen in [(1, 200), (64, 4096), (8, 131072), (128, 8192)]:
+            ws = c.decode_workspace_bytes(0, B, maxlen)
+            assert ws % 4 == 0
+            if ws:
+                # partial outputs plus (max, sum) per split: a multiple of one row per (b, head)
+                rows = B * 8
+                per_split = D * 4 + 8
+                assert (ws - 256) <= rows * per_split * ((maxlen + 15) // 16) + 256
+    assert c.decode_workspace_bytes(0, 0, 100) == 0

@@ -1,0 +1,159 @@
+"""Decode parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases compare every output; the full-size workloads compare sampled
+sequences (every query head of each, every layer) in the launch
+configuration the benchmark times.  Tolerance for bf16 outputs: max-abs
+1e-2 and relative L2 2e-2 against the float64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from paged_case import DecodeCase, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def lay(kind, D, hq, hkv, Wn=0, src=W.KV_OWN):
+    return W.layer(kind, D, hq, hkv, Wn, src)
+
+
+def check_layers(case, seqs, layers=None, lse_tol=2e-3):
+    case.store_current()
+    for i in (range(len(case.layers)) if layers is None else layers):
+        out, lse = case.decode(i)
+        ref, ref_lse = case.oracle_decode(i, seqs)
+        assert_close(out[list(seqs)], ref, what=f"layer {i}")
+        g = lse[list(seqs)].double().cpu().numpy()
+        assert np.all(np.abs(g - ref_lse) <= lse_tol * np.maximum(1.0, np.abs(ref_lse))), f"lse layer {i}"
+    fa = case.fa
+    assert fa.device_error() == 0
+
+
+def test_tiny_decode_workload():
+    w = W.tiny_decode()
+    case = DecodeCase(w.layers, W.seq_lens(w), w.page_size, w.kv_dtype, w.seed, min_pool=w.min_pool_pages)
+    assert case.src == [0, 1, 0]
+    check_layers(case, range(case.B))
+
+
+SMALL = [
+    # (kind, D, hq, hkv, W, lens)
+    (W.FULL, 512, 8, 1, 0, [1, 2, 15, 16, 17, 31, 33, 200, 513]),
+    (W.SLIDING, 256, 8, 1, 64, [1, 16, 63, 64, 65, 66, 80, 81, 300]),
+    (W.SLIDING, 256, 4, 1, 1, [1, 5, 17, 40]),
+    (W.FULL, 256, 16, 2, 0, [7, 100, 257]),
+    (W.SLIDING, 512, 2, 2, 33, [3, 33, 34, 49, 150]),
+    (W.FULL, 512, 8, 8, 0, [20, 64]),
+]
+
+
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("spec", SMALL, ids=[f"{'F' if s[0] == 0 else 'S'}{s[1]}_g{s[2] // s[3]}_W{s[4]}"
+                                             for s in SMALL])
+def test_small_decode(spec, kv_dtype):
+    kind, D, hq, hkv, Wn, lens = spec
+    layers = [lay(kind, D, hq, hkv, Wn), lay(kind, D, hq, hkv, Wn, W.KV_AUTO)]
+    case = DecodeCase(layers, lens, 16, kv_dtype, seed=11, poison=(kv_dtype == W.KV_BF16))
+    check_layers(case, range(case.B))
+
+
+def test_page_size_32_and_zero_length():
+    layers = [lay(W.SLIDING, 256, 8, 1, 40), lay(W.FULL, 512, 8, 1)]
+    lens = [0, 1, 31, 32, 33, 95]
+    case = DecodeCase(layers, [max(1, L) for L in lens], 32, seed=5)
+    case.lens[0] = 0
+    case.lens_dev[0] = 0
+    case.store_current()
+    for i in range(2):
+        out, lse = case.decode(i)
+        assert torch.all(out[0] == 0) and torch.all(torch.isinf(lse[0])) and torch.all(lse[0] < 0)
+        ref, _ = case.oracle_decode(i, range(1, case.B))
+        assert_close(out[1:], ref, what=f"layer {i}")
+
+
+def test_window_one_is_exact_current_value():
+    layers = [lay(W.SLIDING, 256, 8, 1, 1)]
+    case = DecodeCase(layers, [1, 19, 64, 300], 16, seed=9)
+    case.store_current()
+    out, _ = case.decode(0)
+    k, v = case.new_kv[0]
+    assert torch.equal(out, v[:, :1, :].expand_as(out))
+
+
+def test_constant_v_gives_constant_and_permutation_invariance():
+    layers = [lay(W.FULL, 512, 8, 1)]
+    case = DecodeCase(layers, [77, 160, 1000], 16, seed=4)
+    case.store_current()
+    out1, lse1 = case.decode(0)
+    # permute physical pages: move every page p to perm[p], remap the table
+    perm = torch.randperm(case.num_pages, generator=torch.Generator().manual_seed(3)).to("cuda")
+    k_s, v_s, _, _ = case.slabs[0]
+    k2 = torch.empty_like(k_s)
+    v2 = torch.empty_like(v_s)
+    k2[perm] = k_s
+    v2[perm] = v_s
+    k_s.copy_(k2)
+    v_s.copy_(v2)
+    bt = case.bt_dev[0]
+    case.bt_dev[0] = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    out2, lse2 = case.decode(0)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    v_s.fill_(1.0)
+    out3, _ = case.decode(0)
+    assert torch.all(out3 == 1.0)
+
+
+def test_determinism_and_graph_replay():
+    w = W.e2b_decode()
+    layers = w.layers[:5]
+    case = DecodeCase(layers, W.seq_lens(w)[:16], 16, seed=1)
+    case.store_current()
+    outs = [case.decode(i) for i in range(5)]
+    again = [case.decode(i) for i in range(5)]
+    for (a, la), (b, lb) in zip(outs, again):
+        assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_bad_page_id_sets_device_error():
+    """A visible block-table entry outside the pool is skipped (the TMA box
+    then lies outside the tensor and reads zeros) and reported."""
+    layers = [lay(W.FULL, 512, 8, 1)]
+    case = DecodeCase(layers, [40, 50], 16, seed=2)
+    assert case.fa.device_error() == 0
+    case.bt_dev[0][1, 1] = case.num_pages + 5
+    case.decode(0)
+    assert case.fa.device_error() & case.fa.DEV_ERR_PAGE
+    case.bt_dev[0][1, 1] = -1
+    case.decode(0)
+    assert case.fa.device_error() & case.fa.DEV_ERR_PAGE
+    assert case.fa.device_error() == 0
+
+
+# ------------------------------------------------------------------ full size
+def _sample(B, n, seed):
+    return sorted(np.random.default_rng(seed).choice(B, size=min(n, B), replace=False).tolist())
+
+
+def test_e2b_decode_full_size():
+    w = W.e2b_decode()
+    case = DecodeCase(w.layers, W.seq_lens(w), w.page_size, w.kv_dtype, w.seed, poison=True)
+    assert case.src[7:] == [6, 6, 4, 6, 6]
+    lens = case.lens
+    seqs = sorted(set(_sample(case.B, 5, 1) + [int(np.argmax(lens)), int(np.argmin(lens))]))
+    check_layers(case, seqs)
+
+
+def test_long_context_decode_full_size():
+    w = W.long_decode()
+    case = DecodeCase(w.layers, W.seq_lens(w), w.page_size, w.kv_dtype, w.seed, window_table=True, poison=True)
+    check_layers(case, _sample(case.B, 3, 3), layers=[0, 4, 7, 9])
+
+
+def test_int8_decode_full_size():
+    w = W.int8_decode()
+    case = DecodeCase(w.layers, W.seq_lens(w), w.page_size, w.kv_dtype, w.seed)
+    lens = case.lens
+    seqs = sorted(set(_sample(case.B, 4, 5) + [int(np.argmax(lens))]))
+    check_layers(case, seqs)

@@ -171,8 +171,10 @@ def plan_pages(lens: np.ndarray, page_size: int, seed: int, pool_factor: float =
 
 def decode_slot_mapping(lens: np.ndarray, block_table: np.ndarray, page_size: int) -> np.ndarray:
     """Slot of the current token (position L-1) of each sequence: page * ps + off."""
-    out = np.empty(len(lens), dtype=np.int32)
+    out = np.full(len(lens), -1, dtype=np.int32)   # -1: nothing to store (empty sequence)
     for b, L in enumerate(lens):
+        if int(L) <= 0:
+            continue
         pos = int(L) - 1
         out[b] = block_table[b, pos // page_size] * page_size + pos % page_size
     return out
