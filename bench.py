@@ -1,0 +1,574 @@
+"""Benchmark: paged decode attention (and chunked prefill) on GB300.
+
+One step = one decode step of the E2B-like workload through every layer:
+the KV store of the new token on the 7 owning layers, then paged decode
+attention on all 12 layers (7 owning + 5 KV-shared), batch 64, contexts
+U[512, 4096], 8 query heads / 1 KV head, sliding D 256 W 512 / full D 512.
+
+Prints one JSON line.  `value` is the achieved HBM bandwidth of the step:
+algorithmic bytes (KV the layers must read + q + out + the store's rows)
+divided by the device time of the step.  L2 is flushed (256 MiB write)
+before every timed step.  Inputs are seeded synthetic N(0,1) bf16.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the only other place this file runs the oracle).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes
+# ----------------------------------------------------------------------------
+
+def visible(L, d):
+    return min(int(L), d["window"]) if d["kind"] == W.SLIDING else int(L)
+
+
+def decode_bytes(d, lens, kv_dtype):
+    """Bytes a decode launch must move: K and V rows of every visible key
+    (plus the fp32 scales in int8), the queries, the bf16 outputs and lse."""
+    elem = 1 if kv_dtype == W.KV_INT8 else 2
+    per_tok = d["num_kv_heads"] * 2 * (d["head_dim"] * elem + (4 if kv_dtype == W.KV_INT8 else 0))
+    kv = sum(visible(L, d) for L in lens) * per_tok
+    B = len(lens)
+    qo = B * d["num_q_heads"] * (2 * d["head_dim"] * 2 + 4)
+    return kv + qo
+
+
+def store_bytes(d, B, kv_dtype):
+    row_in = d["num_kv_heads"] * d["head_dim"] * 2
+    row_out = d["num_kv_heads"] * (d["head_dim"] * (1 if kv_dtype == W.KV_INT8 else 2) +
+                                   (4 if kv_dtype == W.KV_INT8 else 0))
+    return B * 2 * (row_in + row_out) + B * 4
+
+
+# ----------------------------------------------------------------------------
+# environment helpers
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_digest(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "full_attention_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag, digest):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel source that is built now (else None)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel_tag}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.split(":", 1)[0].strip() in ("source_digest", "dram_bytes_per_launch"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != digest or "dram_bytes_per_launch" not in vals:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except ValueError:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# the decode step on the GPU
+# ----------------------------------------------------------------------------
+
+class DecodeStep:
+    def __init__(self, w: W.DecodeWorkload, device, seed_offset=0):
+        import torch
+        import full_attention_gb300 as fa
+        self.torch, self.fa = torch, fa
+        self.w = w
+        self.layers = w.layers
+        self.lens = W.seq_lens(w)
+        self.B = len(self.lens)
+        self.max_len = int(self.lens.max())
+        self.device = device
+        full = W.plan_pages(self.lens, w.page_size, w.seed)
+        self.tables = {}
+        num_pages = full.num_pages
+        for i, d in enumerate(self.layers):
+            if d["kind"] == W.SLIDING and w.sliding_window_table:
+                p = W.plan_pages(self.lens, w.page_size, w.seed + 1000, window=d["window"],
+                                 max_pages=full.block_table.shape[1])
+            else:
+                p = full
+            self.tables[i] = p.block_table
+            num_pages = max(num_pages, p.num_pages)
+        self.cache = fa.Cache(self.layers, num_pages, w.page_size, w.kv_dtype)
+        self.src = [self.cache.source(i) for i in range(len(self.layers))]
+        self.slabs = self.cache.allocate(device)
+        s0 = 1000 * (seed_offset + 1) + w.seed
+        for i, (k, v, ks, vs) in self.slabs.items():
+            if w.kv_dtype == W.KV_BF16:
+                k.copy_(W.randn_bf16(tuple(k.shape), s0 + 2 * i, device))
+                v.copy_(W.randn_bf16(tuple(v.shape), s0 + 2 * i + 1, device))
+            else:
+                self._fill_int8(i, s0)
+        self.bt = {i: torch.from_numpy(t).to(device) for i, t in self.tables.items()}
+        self.lens_dev = torch.from_numpy(self.lens).to(device)
+        self.q, self.out, self.lse, self.ws = {}, {}, {}, {}
+        for i, d in enumerate(self.layers):
+            self.q[i] = W.randn_bf16((self.B, d["num_q_heads"], d["head_dim"]), s0 + 100 + i, device)
+            self.out[i] = torch.empty((self.B, d["num_q_heads"], d["head_dim"]), dtype=torch.bfloat16, device=device)
+            self.lse[i] = torch.empty((self.B, d["num_q_heads"]), dtype=torch.float32, device=device)
+            n = self.cache.decode_workspace_bytes(i, self.B, self.max_len)
+            self.ws[i] = fa.workspace(n, device) if n else None
+        self.new = {}
+        for i in self.slabs:
+            d = self.layers[i]
+            sl = torch.from_numpy(W.decode_slot_mapping(self.lens, self.tables[i], w.page_size)).to(device)
+            self.new[i] = (W.randn_bf16((self.B, d["num_kv_heads"], d["head_dim"]), s0 + 200 + i, device),
+                           W.randn_bf16((self.B, d["num_kv_heads"], d["head_dim"]), s0 + 300 + i, device), sl)
+        self.decode_bytes = [decode_bytes(d, self.lens, w.kv_dtype) for d in self.layers]
+        self.store_bytes = sum(store_bytes(self.layers[i], self.B, w.kv_dtype) for i in self.slabs)
+        self.step_bytes = sum(self.decode_bytes) + self.store_bytes
+        torch.cuda.synchronize()
+
+    def _fill_int8(self, i, s0):
+        torch = self.torch
+        d = self.layers[i]
+        slots = []
+        for b, L in enumerate(self.lens):
+            lo = max(0, int(L) - d["window"]) if d["kind"] == W.SLIDING else 0
+            slots.append(W.slots_for_positions(self.tables[i][b], np.arange(lo, int(L)), self.w.page_size))
+        sl = torch.from_numpy(np.concatenate(slots)).to(self.device)
+        for c0 in range(0, sl.numel(), 1 << 18):
+            part = sl[c0:c0 + (1 << 18)]
+            k = W.randn_bf16((part.numel(), d["num_kv_heads"], d["head_dim"]), s0 + 7 * i + c0, self.device)
+            v = W.randn_bf16((part.numel(), d["num_kv_heads"], d["head_dim"]), s0 + 7 * i + c0 + 1, self.device)
+            self.cache.store(i, k, v, part)
+
+    def launches_per_step(self):
+        n = 0
+        for i, d in enumerate(self.layers):
+            if self.src[i] == i:
+                n += 1
+            n += 2 if self.ws[i] is not None else 1
+        return n
+
+    def run(self, events=None):
+        for i in range(len(self.layers)):
+            if self.src[i] == i:
+                k, v, sl = self.new[i]
+                self.cache.store(i, k, v, sl)
+            if events is not None:
+                events[i][0].record()
+            self.cache.decode(i, self.q[i], self.bt[i], self.lens_dev, self.max_len, self.out[i], self.lse[i],
+                              self.ws[i])
+            if events is not None:
+                events[i][1].record()
+
+
+def gpu_arm(args, rank, world):
+    import torch
+    import full_attention_gb300 as fa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = W.ALL[args.workload]()
+    step = DecodeStep(w, dev, seed_offset=rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    nl = len(step.layers)
+    events = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nl)]
+    graph = None
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step.run(events)
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step.run(events)
+        torch.cuda.synchronize()
+    except Exception as e:   # capture unsupported: time eager launches
+        print(f"# graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        graph = None
+        torch.cuda.synchronize()
+    st0, st1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, dec_ms = [], [0.0] * nl
+    gpu_idx = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None) or dev.index
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(gpu_idx) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            st0.record()
+            if graph is not None:
+                graph.replay()
+            else:
+                step.run(events)
+            st1.record()
+            st1.synchronize()
+            step_ms.append(st0.elapsed_time(st1))
+            for i in range(nl):
+                dec_ms[i] += events[i][0].elapsed_time(events[i][1])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    assert fa.device_error() == 0
+    t_step = sum(step_ms) / len(step_ms) / 1e3       # seconds per step (device time)
+    t_tot = torch.tensor([sum(step_ms)], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_tot, op=torch.distributed.ReduceOp.MAX)
+    t_max = float(t_tot.item()) / 1e3 / args.steps
+    hbm, bf16, bf16s, peak_src = measured_peaks()
+    dec_bytes = sum(step.decode_bytes)
+    dec_time = sum(dec_ms) / 1e3 / args.steps         # seconds of decode launches per step
+    per_kind = {}
+    for kind, name in ((W.FULL, "full"), (W.SLIDING, "sliding")):
+        idx = [i for i, d in enumerate(step.layers) if d["kind"] == kind]
+        b = sum(step.decode_bytes[i] for i in idx)
+        t = sum(dec_ms[i] for i in idx) / 1e3 / args.steps
+        per_kind[name] = {"launches_per_step": len(idx), "gb_per_s": round(b / t / 1e9, 1) if t else None,
+                          "us_per_launch": round(t / len(idx) * 1e6, 2) if idx else None}
+    achieved = dec_bytes / dec_time / 1e9
+    digest = source_digest("fa_decode.cu", "fa_ptx.cuh")
+    traffic = profiled_traffic(f"decode_{args.workload}", digest)
+    clocks = clk.summary()
+    res = {
+        "metric": "paged decode-attn achieved HBM GB/s (% of peak); chunked-prefill TFLOP/s",
+        "value": round(step.step_bytes * world / t_max / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == W.KV_BF16 else "int8",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name, "batch": step.B, "layers": nl, "page_size": w.page_size,
+                   "max_ctx": step.max_len, "l2": "flushed before every step (256 MiB write)",
+                   "graph": graph is not None, "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(step.B * world / t_max, 1),
+        "pct_of_peak": round(100 * step.step_bytes / t_max / 1e9 / hbm, 1),
+        "roofline": {"kernel": "paged decode attention (split-K kernel + LSE combine, one C call)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 3), "peak_source": peak_src,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": round(dec_bytes / nl),
+                     "per_kind": per_kind},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0:
+        res["e2e"] = e2e_decode(step, args, torch)
+        if args.workload == "e2b_decode" and not args.no_prefill:
+            res["prefill"] = prefill_measure(args, dev)
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+
+
+def e2e_decode(step, args, torch):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs (queries, new k/v rows, slots, lengths, tables) from pinned
+    host memory and reads every layer's output back."""
+    dev = step.device
+    h_q = {i: t.cpu().pin_memory() for i, t in step.q.items()}
+    h_new = {i: tuple(x.cpu().pin_memory() for x in t) for i, t in step.new.items()}
+    h_bt = {i: t.cpu().pin_memory() for i, t in step.bt.items()}
+    h_lens = step.lens_dev.cpu().pin_memory()
+    h_out = {i: torch.empty_like(t, device="cpu").pin_memory() for i, t in step.out.items()}
+    bi = sum(t.numel() * t.element_size() for t in h_q.values()) + \
+        sum(x.numel() * x.element_size() for t in h_new.values() for x in t) + \
+        sum(t.numel() * t.element_size() for t in h_bt.values()) + h_lens.numel() * 4
+    bo = sum(t.numel() * t.element_size() for t in h_out.values())
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(args.steps, 200))
+    tot = 0.0
+    for it in range(n + 2):
+        flush.zero_()
+        e0.record()
+        for i in h_q:
+            step.q[i].copy_(h_q[i], non_blocking=True)
+        for i in h_new:
+            for dst, src in zip(step.new[i], h_new[i]):
+                dst.copy_(src, non_blocking=True)
+        for i in h_bt:
+            step.bt[i].copy_(h_bt[i], non_blocking=True)
+        step.lens_dev.copy_(h_lens, non_blocking=True)
+        step.run()
+        for i in h_out:
+            h_out[i].copy_(step.out[i], non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if it >= 2:
+            tot += e0.elapsed_time(e1)
+    t = tot / n / 1e3
+    return {"value": round(step.step_bytes / t / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": int(bi),
+            "d2h_bytes_per_step": int(bo), "ms_per_step": round(t * 1e3, 4), "path": "eager C-ABI calls"}
+
+
+def prefill_measure(args, dev):
+    """Chunked prefill TFLOP/s on the chunked-prefill workload (extend kernel)."""
+    return {"status": "extend kernel not built yet"}
+
+
+# ----------------------------------------------------------------------------
+# oracle (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def _bf16_normal(r, shape):
+    """Seeded N(0,1) values as bf16 bit patterns (input generation, CPU)."""
+    x = r.standard_normal(shape, dtype=np.float32).view(np.uint32)
+    return ((x + 0x7FFF + ((x >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _oracle_worker(conn, name, units, seed):
+    """A spawned process that holds seeded inputs for its (sequence, layer)
+    units and, on each request, runs the oracle on the next n of them; only
+    the oracle calls are timed."""
+    import oracle
+    w = W.ALL[name]()
+    lens = W.seq_lens(w)
+    ps = w.page_size
+    r = W.rng(seed)
+    data = []
+    for b, li in units:
+        d = dict(w.layers[li], kv_source=W.KV_OWN)
+        L = int(lens[b])
+        npg = (L + ps - 1) // ps
+        shape = (npg, d["num_kv_heads"], ps, d["head_dim"])
+        if w.kv_dtype == W.KV_BF16:
+            slab = (_bf16_normal(r, shape), _bf16_normal(r, shape))
+        else:
+            sc = (r.random(shape[:3], dtype=np.float32) * 0.03).astype(np.float32)
+            slab = (r.integers(-127, 128, size=shape, dtype=np.int8), r.integers(-127, 128, size=shape, dtype=np.int8),
+                    sc, sc.copy())
+        q = _bf16_normal(r, (1, d["num_q_heads"], d["head_dim"]))
+        data.append((d, slab, q, np.arange(npg, dtype=np.int32)[None], np.array([L], np.int32),
+                     decode_bytes(d, [L], w.kv_dtype)))
+    conn.send("ready")
+    k = 0
+    while True:
+        n = conn.recv()
+        if n is None:
+            break
+        t = 0.0
+        nb = 0
+        for _ in range(n):
+            d, slab, q, bt, L, by = data[k % len(data)]
+            k += 1
+            t0 = time.perf_counter()
+            oracle.paged_decode([d], 0, {0: slab}, q, bt, L, ps)
+            t += time.perf_counter() - t0
+            nb += by
+        conn.send((t, nb))
+
+
+class OraclePool:
+    """One spawned oracle process per host core, each owning a share of the
+    workload's (sequence, layer) units.  Spawned, never forked, so it is safe
+    after CUDA is initialised."""
+
+    def __init__(self, name, procs=None, seed=0):
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"   # one thread per process: `cores` counts processes
+        w = W.ALL[name]()
+        B = len(W.seq_lens(w))
+        units = [(b, li) for b in range(B) for li in range(len(w.layers))]
+        self.procs = max(1, min(procs or os.cpu_count() or 1, len(units)))
+        self.units = len(units)
+        ctx = mp.get_context("spawn")
+        self.conns, self.ps = [], []
+        for i in range(self.procs):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(b, name, units[i::self.procs], seed + i), daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.ps.append(p)
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def run(self, n_per_proc):
+        """Every process runs n units; returns (bytes, busy seconds = max over processes)."""
+        for c in self.conns:
+            c.send(int(n_per_proc))
+        res = [c.recv() for c in self.conns]
+        return sum(b for _, b in res), max(t for t, _ in res)
+
+    def close(self):
+        for c in self.conns:
+            c.send(None)
+        for p in self.ps:
+            p.join(timeout=10)
+
+
+def cpu_baseline(name, seconds):
+    """The oracle on the whole decode step (every sequence, every layer), one
+    process per core, repeated until about `seconds` of oracle time."""
+    pool = OraclePool(name)
+    try:
+        per = -(-pool.units // pool.procs)
+        nb, t = pool.run(per)
+        reps = 1
+        while t < seconds / 4 and reps < 8:
+            b2, t2 = pool.run(per)
+            nb, t, reps = nb + b2, t + t2, reps + 1
+    finally:
+        pool.close()
+    w = W.ALL[name]()
+    return {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": pool.procs, "kind": "oracle",
+            "sample": f"the whole step ({len(W.seq_lens(w))} sequences x {len(w.layers)} layers) x {reps}, "
+                      f"fp64 numpy oracle, {pool.procs} processes, {t:.2f} s of oracle wall time"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    w = W.ALL[args.workload]()
+    pool = OraclePool(args.workload)
+    try:
+        _, t1 = pool.run(1)                       # one unit per process: sizes the step
+        budget = 150.0                            # seconds for the whole run
+        n = max(1, int(min(1.0, budget / (args.steps + args.warmup)) / max(t1, 1e-4)))
+        for _ in range(args.warmup):
+            pool.run(n)
+        nb = t = 0.0
+        for _ in range(args.steps):
+            b, dt = pool.run(n)
+            nb += b
+            t += dt
+    finally:
+        pool.close()
+    value = round(nb / t / 1e9, 4)
+    sample = f"{n} (sequence, layer) units per process per step, {pool.procs} processes, fp64 numpy oracle"
+    res = {"impl": "reference", "metric": "paged decode-attn achieved HBM GB/s (% of peak); chunked-prefill TFLOP/s",
+           "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": w.name, "sample_per_step": sample},
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.procs, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="e2b_decode", choices=["e2b_decode", "long_decode", "int8_decode",
+                                                                  "tiny_decode"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        gpu_arm(args, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

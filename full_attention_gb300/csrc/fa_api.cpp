@@ -5,6 +5,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -58,25 +59,33 @@ DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len) {
     if (win_tiles < tiles) tiles = win_tiles;
   }
   p.max_tiles = tiles;
-  // tiles per pipeline step: a step moves 32 KB of K and V
+  p.units = B * d.num_kv_heads * p.head_chunks;
+  // a pipeline step moves 32 KB of K and V; a CTA gets at least 4 steps
   const int tile_bytes = 2 * kTile * d.head_dim * static_cast<int>(elem_bytes(c->kv_dtype));
-  const int nt = 32768 / tile_bytes;
-  const int min_tps = 4 * nt;
-  const long units = static_cast<long>(B) * d.num_kv_heads * p.head_chunks;
-  const long target = 4L * 2 * sm_count();   // ~4 waves of 2 resident CTAs per SM
-  long splits = (target + units - 1) / units;
-  if (splits < 1) splits = 1;
-  long tps = (tiles + splits - 1) / splits;
-  if (tps < min_tps) tps = min_tps;
-  if (tps > 512) tps = 512;   // the CTA keeps its page ids in shared memory
-  tps = (tps + nt - 1) / nt * nt;
-  p.tiles_per_split = static_cast<int>(tps);
-  p.splits = static_cast<int>((tiles + tps - 1) / tps);
-  const size_t rows = static_cast<size_t>(B) * d.num_q_heads * p.splits;
-  p.o_bytes = rows * d.head_dim * sizeof(float);
-  p.ml_bytes = rows * 2 * sizeof(float);
-  p.ws_bytes = (p.splits > 1) ? ((p.o_bytes + 255) / 256 * 256 + p.ml_bytes) : 0;
+  p.min_tiles = 4 * (32768 / tile_bytes);
+  const long long t_bound = static_cast<long long>(p.units) * tiles;
+  const long long slots = 2LL * sm_count();   // two resident CTAs per SM
+  long long n = (t_bound + p.min_tiles - 1) / p.min_tiles;
+  if (n > slots) n = slots;
+  if (n < 1) n = 1;
+  p.ncta = static_cast<int>(n);
+  if (p.ncta > 1) {
+    const size_t rows = static_cast<size_t>(p.ncta + p.units) * 8;   // partial slots x heads
+    p.off_prefix = 256;
+    p.off_ml = p.off_prefix + (static_cast<size_t>(p.units) * 4 + 255) / 256 * 256;
+    p.off_o = p.off_ml + (rows * 2 * sizeof(float) + 255) / 256 * 256;
+    p.ws_bytes = p.off_o + rows * d.head_dim * sizeof(float);
+  }
   return p;
+}
+
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("FA_PDL");
+    on = (e && e[0] == '0') ? 0 : 1;
+  }
+  return on == 1;
 }
 
 // ------------------------------------------------------------ TMA encoding
@@ -362,7 +371,6 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
     return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_seq_len %d", max_pages_per_seq,
                 max_seq_len);
   DecodePlan p = plan_decode(c, layer, B, max_seq_len);
-  if (p.splits > 65535) return fail(FA_ERR_UNSUPPORTED, "too many splits");
   if (workspace_bytes < p.ws_bytes || (p.ws_bytes && !workspace))
     return fail(FA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, p.ws_bytes);
   if (p.ws_bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -378,9 +386,7 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.v_scale = s->v_scale;
   a.out = out;
   a.lse = lse;
-  a.o_part = static_cast<float*>(workspace);
-  a.ml_part = p.ws_bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + (p.o_bytes + 255) / 256 * 256)
-                         : nullptr;
+  a.workspace = p.ws_bytes ? workspace : nullptr;
   a.tm_k = &s->tm_k;
   a.tm_v = &s->tm_v;
   a.tm_ks = &s->tm_ks;

@@ -59,16 +59,38 @@ int sm_count();
 cudaError_t set_smem_once(const void* fn, int bytes, unsigned int* done_mask);
 
 // ---------------------------------------------------------------- decode plan
+// The decode kernel splits the concatenated tile lists of all (sequence, KV
+// head, head chunk) units evenly over at most `ncta` CTAs; a unit whose tiles
+// land on one CTA is finished there, the others are merged by a combine pass.
 struct DecodePlan {
   int head_chunks = 1;      // ceil(g / 8): query heads are packed 8 per MMA column block
-  int max_tiles = 0;        // 16-row tiles a sequence can touch under the bound
-  int tiles_per_split = 0;  // tiles one CTA walks
-  int splits = 0;           // CTAs per (sequence, KV head, head chunk)
-  size_t o_bytes = 0;       // partial outputs: float [B][Hq][splits][D]
-  size_t ml_bytes = 0;      // partial (max, sum): float [B][Hq][splits][2]
+  int units = 0;            // B * Hkv * head_chunks
+  int max_tiles = 0;        // 16-row tiles a unit can touch under the length bound
+  int min_tiles = 0;        // fewest tiles a CTA is given
+  int ncta = 0;             // CTAs launched
+  size_t off_prefix = 0, off_ml = 0, off_o = 0;   // workspace layout (bytes)
   size_t ws_bytes = 0;
 };
 DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len);
+
+// Launch with programmatic stream serialisation (overlaps launch latency with
+// the previous kernel's tail); every kernel waits on griddepcontrol first.
+bool pdl_enabled();
+
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 struct StoreArgs {
   const void* k;
@@ -91,8 +113,7 @@ struct DecodeArgs {
   const float* v_scale;
   void* out;
   float* lse;
-  float* o_part;
-  float* ml_part;
+  void* workspace;
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_ks;

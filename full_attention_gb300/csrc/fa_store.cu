@@ -42,6 +42,8 @@ unsigned int* device_error_word(cudaError_t* err) {
 
 template <int D>
 __global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int rows = a.T * a.Hkv * 2;
@@ -76,6 +78,8 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&x)[8]) {
 template <int D>
 __global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
   constexpr int NV = D / 256;            // 16-byte vectors (8 values) per lane
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int rows = a.T * a.Hkv * 2;
@@ -128,14 +132,12 @@ cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {
   const int block = 256;
   const long grid = (warps * 32 + block - 1) / block;
   if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
-  if (a.kv_dtype == FA_KV_INT8) {
-    if (a.D == 256) store_int8_kernel<256><<<grid, block, 0, s>>>(a);
-    else store_int8_kernel<512><<<grid, block, 0, s>>>(a);
-  } else {
-    if (a.D == 256) store_bf16_kernel<256><<<grid, block, 0, s>>>(a);
-    else store_bf16_kernel<512><<<grid, block, 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  const dim3 g(static_cast<unsigned>(grid)), b(block);
+  if (a.kv_dtype == FA_KV_INT8)
+    return a.D == 256 ? launch_pdl(store_int8_kernel<256>, g, b, 0, s, a)
+                      : launch_pdl(store_int8_kernel<512>, g, b, 0, s, a);
+  return a.D == 256 ? launch_pdl(store_bf16_kernel<256>, g, b, 0, s, a)
+                    : launch_pdl(store_bf16_kernel<512>, g, b, 0, s, a);
 }
 
 }  // namespace fa

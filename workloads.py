@@ -22,7 +22,6 @@ import math
 from dataclasses import dataclass, field
 
 import numpy as np
-import torch
 
 FULL = 0
 SLIDING = 1
@@ -185,13 +184,15 @@ def slots_for_positions(block_table_row: np.ndarray, positions: np.ndarray, page
     return (pages * page_size + positions % page_size).astype(np.int32)
 
 
-def randn_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
+def randn_bf16(shape, seed: int, device="cpu"):
     """N(0,1) values rounded to bf16, from a seeded torch generator."""
+    import torch
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
-def bf16_bits(t: torch.Tensor) -> np.ndarray:
+def bf16_bits(t) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (what the oracle reads)."""
+    import torch
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
