@@ -18,7 +18,9 @@ LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
 FULL, SLIDING = 0, 1
 KV_BF16, KV_INT8 = 0, 1
 KV_OWN, KV_AUTO = -1, -2
-DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT = 1, 2, 4, 8
+DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE = 1, 2, 4, 8, 16
+
+FLAG_EARLY_METADATA = 1
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NOT_BOUND, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4, 5
 
@@ -43,6 +45,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "fa_cache_create": (i32, [ctypes.POINTER(LayerDesc), i32, i32, i32, i32, ctypes.POINTER(vp)]),
         "fa_cache_destroy": (None, [vp]),
+        "fa_cache_set_flags": (i32, [vp, ctypes.c_uint32]),
         "fa_cache_layer_source": (i32, [vp, i32, ctypes.POINTER(i32)]),
         "fa_cache_slab_bytes": (i32, [vp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "fa_cache_bind_slab": (i32, [vp, i32, vp, vp, vp, vp]),
@@ -112,6 +115,11 @@ class Cache:
         if h is not None and _lib is not None:
             _lib.fa_cache_destroy(h)
             self._h = None
+
+    def set_flags(self, flags: int) -> None:
+        """FA_FLAG_* options; FLAG_EARLY_METADATA lets kernels read index
+        arrays before the previous kernel in the stream has finished."""
+        _check(_lib.fa_cache_set_flags(self._h, int(flags)))
 
     def source(self, layer: int) -> int:
         out = ctypes.c_int32()
@@ -183,5 +191,6 @@ def device_error(stream=None) -> int:
 
 
 def workspace(nbytes: int, device="cuda"):
-    """A 256-byte-aligned scratch buffer of at least nbytes (torch-allocated)."""
-    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+    """A zeroed, 256-byte-aligned decode workspace of at least nbytes
+    (torch-allocated; decode calls leave its counters zero for reuse)."""
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)

@@ -71,8 +71,7 @@ DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len) {
   p.ncta = static_cast<int>(n);
   if (p.ncta > 1) {
     const size_t rows = static_cast<size_t>(p.ncta + p.units) * 8;   // partial slots x heads
-    p.off_prefix = 256;
-    p.off_ml = p.off_prefix + (static_cast<size_t>(p.units) * 4 + 255) / 256 * 256;
+    p.off_ml = (static_cast<size_t>(p.units) * 4 + 255) / 256 * 256;
     p.off_o = p.off_ml + (rows * 2 * sizeof(float) + 255) / 256 * 256;
     p.ws_bytes = p.off_o + rows * d.head_dim * sizeof(float);
   }
@@ -255,6 +254,13 @@ fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t
 
 void fa_cache_destroy(fa_cache* c) { delete c; }
 
+fa_status fa_cache_set_flags(fa_cache* c, uint32_t flags) {
+  if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
+  if (flags & ~static_cast<uint32_t>(FA_FLAG_EARLY_METADATA)) return fail(FA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  c->flags = flags;
+  return ok();
+}
+
 fa_status fa_cache_layer_source(const fa_cache* c, int32_t layer, int32_t* slab_owner) {
   fa_status st = check_layer(c, layer);
   if (st) return st;
@@ -341,7 +347,7 @@ fa_status fa_kv_store(fa_cache* c, int32_t layer, const void* k, const void* v, 
   unsigned int* err = device_error_word(&ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   StoreArgs a{k, v, slot_mapping, s->k, s->v, s->k_scale, s->v_scale, T, L.d.num_kv_heads, L.d.head_dim,
-              c->page_size, c->num_pages, c->kv_dtype, err};
+              c->page_size, c->num_pages, c->kv_dtype, (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0, err};
   ce = launch_store(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "store launch: %s", cudaGetErrorString(ce));
   return ok();
@@ -402,6 +408,7 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.max_pages_per_seq = max_pages_per_seq;
   a.max_seq_len = max_seq_len;
   a.kv_dtype = c->kv_dtype;
+  a.early_metadata = (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0;
   a.sm_scale = L.d.sm_scale;
   a.plan = p;
   a.err = err;

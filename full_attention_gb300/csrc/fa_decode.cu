@@ -14,7 +14,8 @@
 // the same number of bytes whatever the length mix.  A CTA walks its share
 // unit segment by unit segment without draining its pipeline.  A unit whose
 // tiles all fall on one CTA is finished there; the others leave per-CTA
-// partial (max, sum, o) rows that a combine pass merges.
+// partial (max, sum, o) rows, and the last of their CTAs to arrive (counted
+// by an atomic per unit in the workspace) merges them.
 //
 // Per tile the contraction is
 //   S^T (16 keys x 8 heads)  = K (16 x D) . Q^T (D x 8)         (mma.sync m16n8k16)
@@ -72,13 +73,12 @@ struct DecK {
   const int32_t* seq_lens;
   __nv_bfloat16* out;
   float* lse;
-  int* ws_hdr;      // [0] total tiles T, [1] CTAs used (null: no workspace, one CTA)
-  int* ws_prefix;   // [U] first global tile of each unit
+  int* counters;    // [U] arrival count per unit (null: no workspace, one CTA); zero between calls
   float* ml_part;   // [(ncta + U) * 8][2]
   float* o_part;    // [(ncta + U) * 8][D]
   unsigned int* err;
   int B, Hq, Hkv, g, chunks, kind, window, page_size, tiles_per_page, num_pages, max_pages_per_seq;
-  int max_seq_len, units, min_tiles;
+  int max_seq_len, units, min_tiles, early_metadata;
   float scale_log2;   // sm_scale * log2(e)
 };
 
@@ -141,6 +141,124 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sm, int* total) {
   return base + incl - v;
 }
 
+// Sequences of length <= 0 get out = 0 and lse = -inf; CTA `cta` of `ncta`
+// writes the units u with u % ncta == cta.
+template <int D>
+__device__ void zero_empty_units(const DecK& p, int cta, int ncta, int tid, int nthr) {
+  for (int u = cta; u < p.units; u += ncta) {
+    const Unit x = unit_of(p, u);
+    if (x.L > 0) continue;
+    const int nh = min(8, p.g - x.c * 8), head0 = x.h * p.g + x.c * 8;
+    for (int i = tid; i < nh * D; i += nthr)
+      p.out[(static_cast<size_t>(x.b) * p.Hq + head0 + i / D) * D + i % D] = __float2bfloat16(0.0f);
+    if (p.lse && tid < nh) p.lse[static_cast<size_t>(x.b) * p.Hq + head0 + tid] = -INFINITY;
+  }
+}
+
+// Merge the partial rows of unit u that CTAs cf..cl left (this CTA arrived
+// last): per head h, M = max_c m_c, L = sum_c l_c 2^(m_c - M) and
+// out = sum_c o_c 2^(m_c - M) / L, lse = (M + log2 L) ln 2.  Run by the 128
+// consumer threads; wbuf is shared scratch of 8 * 128 + 16 floats.  Loads are
+// batched so that a typical merge (a handful of source CTAs) costs a few L2
+// round trips.
+template <int D>
+__device__ void merge_unit(const DecK& p, int u, const Unit& x, int nh, int head0, int cf, int cl, float* wbuf) {
+  constexpr int CH = 128;                  // source CTAs per weight chunk
+  constexpr int ITEMS = 8 * (D / 4) / 128; // float4 outputs per thread
+  const int tid = threadIdx.x;
+  const int nct = cl - cf + 1;
+  const float2* mlg = reinterpret_cast<const float2*>(p.ml_part);
+  float* Mh = wbuf + 8 * CH;
+  float* Lh = Mh + 8;
+  const int h = tid >> 4, k = tid & 15;    // 16 threads per head
+  // one pass: running max with rescaled sum; the first 64 pairs stay in
+  // registers for the weights
+  float M = -INFINITY, L = 0.f;
+  float2 v[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = k + 16 * r;
+    v[r] = c < nct ? __ldcg(mlg + (static_cast<size_t>(cf + c) + u) * 8 + h) : make_float2(-INFINITY, 0.f);
+  }
+  auto fold = [&](float2 x) {
+    if (x.x == -INFINITY) return;
+    const float Mn = fmaxf(M, x.x);
+    L = L * ex2(M - Mn) + x.y * ex2(x.x - Mn);
+    M = Mn;
+  };
+#pragma unroll
+  for (int r = 0; r < 4; ++r) fold(v[r]);
+  for (int c = k + 64; c < nct; c += 16) fold(__ldcg(mlg + (static_cast<size_t>(cf + c) + u) * 8 + h));
+  // combine the 16 threads of the head
+#pragma unroll
+  for (int o = 8; o; o >>= 1) {
+    const float Mo = __shfl_xor_sync(0xffffffffu, M, o), Lo = __shfl_xor_sync(0xffffffffu, L, o);
+    const float Mn = fmaxf(M, Mo);
+    L = (Mn == -INFINITY) ? 0.f : L * ex2(M - Mn) + Lo * ex2(Mo - Mn);
+    M = Mn;
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = k + 16 * r;
+    if (c < CH) wbuf[c * 8 + h] = (h < nh && c < nct) ? ex2(v[r].x - M) : 0.f;
+  }
+  for (int c = k + 64; c < min(nct, CH); c += 16)
+    wbuf[c * 8 + h] = (h < nh) ? ex2(__ldcg(mlg + (static_cast<size_t>(cf + c) + u) * 8 + h).x - M) : 0.f;
+  if (k == 0) {
+    Mh[h] = M;
+    Lh[h] = L;
+  }
+  named_bar_sync(1, 128);
+  float4 acc[ITEMS];
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < nct; c0 += CH) {
+    const int n = min(CH, nct - c0);
+    if (c0 > 0) {   // weights of later chunks (more than CH source CTAs)
+      named_bar_sync(1, 128);
+      for (int e = tid; e < n * 8; e += 128) {
+        const int c = e >> 3, hh = e & 7;
+        const float m = __ldcg(p.ml_part + (static_cast<size_t>(cf + c0 + c) + u) * 16 + hh * 2);
+        wbuf[e] = (hh < nh) ? ex2(m - Mh[hh]) : 0.f;
+      }
+      named_bar_sync(1, 128);
+    }
+    // source CTAs outer, this thread's outputs inner: every iteration has
+    // ITEMS independent L2 loads in flight
+#pragma unroll 8
+    for (int c = 0; c < n; ++c) {
+      const float* src = p.o_part + (static_cast<size_t>(cf + c0 + c) + u) * 8 * D;
+      float4 o[ITEMS];
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int idx = tid + i * 128, hh = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        o[i] = (hh < nh) ? __ldcg(reinterpret_cast<const float4*>(src + hh * D + d)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const float w = wbuf[c * 8 + (tid + i * 128) / (D / 4)];
+        acc[i].x += w * o[i].x;
+        acc[i].y += w * o[i].y;
+        acc[i].z += w * o[i].z;
+        acc[i].w += w * o[i].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int idx = tid + i * 128, hh = idx / (D / 4), d = (idx % (D / 4)) * 4;
+    if (hh >= nh) continue;
+    const float inv = Lh[hh] > 0.f ? 1.0f / Lh[hh] : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc[i].x * inv, acc[i].y * inv);
+    packed.y = pack_bf16x2(acc[i].z * inv, acc[i].w * inv);
+    *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(x.b) * p.Hq + head0 + hh) * D + d) = packed;
+  }
+  if (p.lse && tid < nh)
+    p.lse[static_cast<size_t>(x.b) * p.Hq + head0 + tid] = (Mh[tid] + __log2f(Lh[tid])) * 0.69314718055994531f;
+  named_bar_sync(1, 128);   // the scratch (the score-exchange buffer) is free again
+}
+
 template <int D, int KV>
 __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -156,52 +274,67 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   uint64_t* qfull = empty + C::NSTAGE;
   uint64_t* qempty = qfull + 1;
   __shared__ int sm_scan[8];
-  __shared__ int sh_u0, sh_p0, abort_flag;
+  __shared__ int sh_u0, sh_p0, abort_flag, sh_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
-  griddep_wait();               // inputs may come from the previous kernel in the stream
+  // Inputs may come from the previous kernel in the stream.  With early
+  // metadata the caller guarantees that kernel writes no block table or
+  // sequence length, so the partition below (and the first page ids) may be
+  // read before waiting for it; q, the slabs and the outputs always wait.
+  if (!p.early_metadata) griddep_wait();
   griddep_launch_dependents();
 
   // ---------------------------------------------------------------- partition
-  int T = 0;
+  // One block scan gives every unit's first global tile P_u and the total T.
+  // When all units fit one pass (the usual case) the unit holding this CTA's
+  // first tile is found from it; otherwise a second pass finds it.
+  int T = 0, my_n = 0, my_P = 0;
   {
-    int part = 0;
-    for (int u = threadIdx.x; u < p.units; u += blockDim.x) {
-      const Unit x = unit_of(p, u);
-      part += x.n;
-      if (x.L <= 0 && (u % gridDim.x) == blockIdx.x) {   // empty sequence: zero output, lse -inf
-        const int nh = min(8, p.g - x.c * 8), head0 = x.h * p.g + x.c * 8;
-        for (int i = 0; i < nh * D; ++i)
-          p.out[(static_cast<size_t>(x.b) * p.Hq + head0 + i / D) * D + i % D] = __float2bfloat16(0.0f);
-        if (p.lse)
-          for (int i = 0; i < nh; ++i) p.lse[static_cast<size_t>(x.b) * p.Hq + head0 + i] = -INFINITY;
+    int running = 0;
+    for (int base = 0; base < p.units; base += blockDim.x) {
+      const int u = base + threadIdx.x;
+      Unit x{};
+      if (u < p.units) {
+        x = unit_of(p, u);
+        if (blockIdx.x == 0 && __ldg(p.seq_lens + x.b) > p.max_seq_len) atomicOr(p.err, FA_DEV_ERR_BOUND);
       }
+      int tot;
+      const int P = running + block_excl_scan(x.n, sm_scan, &tot);
+      if (base == 0) {
+        my_n = x.n;
+        my_P = P;
+      }
+      running += tot;
     }
-    block_excl_scan(part, sm_scan, &T);
+    T = running;
   }
   const int ncta = (T == 0) ? 0 : min(static_cast<int>(gridDim.x), max(1, (T + p.min_tiles - 1) / p.min_tiles));
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.ws_hdr) {
-    p.ws_hdr[0] = T;
-    p.ws_hdr[1] = ncta;
+  if (static_cast<int>(blockIdx.x) >= ncta) {
+    if (ncta == 0 && blockIdx.x == 0) {   // nothing visible anywhere: only empty outputs to write
+      griddep_wait();
+      zero_empty_units<D>(p, 0, 1, threadIdx.x, blockDim.x);
+    }
+    return;
   }
-  if (static_cast<int>(blockIdx.x) >= ncta) return;
   const long long s_beg = static_cast<long long>(blockIdx.x) * T / ncta;
   const long long s_end = static_cast<long long>(blockIdx.x + 1) * T / ncta;
-  {
+  if (p.units <= static_cast<int>(blockDim.x)) {
+    if (my_n > 0 && my_P <= s_beg && s_beg < my_P + my_n) {
+      sh_u0 = threadIdx.x;
+      sh_p0 = my_P;
+    }
+  } else {
     int running = 0;
     for (int base = 0; base < p.units; base += blockDim.x) {
       const int u = base + threadIdx.x;
       const int n = (u < p.units) ? unit_of(p, u).n : 0;
       int tot;
       const int P = running + block_excl_scan(n, sm_scan, &tot);
-      if (u < p.units) {
-        if (blockIdx.x == 0 && p.ws_prefix) p.ws_prefix[u] = P;
-        if (n > 0 && P <= s_beg && s_beg < P + n) {
-          sh_u0 = u;
-          sh_p0 = P;
-        }
+      if (n > 0 && P <= s_beg && s_beg < P + n) {
+        sh_u0 = u;
+        sh_p0 = P;
       }
       running += tot;
     }
@@ -235,14 +368,6 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
         const int ta = x.t_first + static_cast<int>(max(s_beg, P) - P);
         const int tz = x.t_first + static_cast<int>(min(s_end, P + x.n) - P);
         const int nh = min(8, p.g - x.c * 8), head0 = x.h * p.g + x.c * 8;
-        if (lane == 0) {
-          if (j > 0) ok = mbar_wait(qempty, (j - 1) & 1);
-          if (ok) {
-            mbar_arrive_expect_tx(qfull, nh * D * 2);
-            bulk_load(qbuf, p.q + (static_cast<size_t>(x.b) * p.Hq + head0) * D, nh * D * 2, qfull);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
         const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
         for (int k0 = ta; ok && k0 < tz; k0 += 32) {
           int pid = -1;
@@ -252,6 +377,18 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
               atomicOr(p.err, FA_DEV_ERR_PAGE);
               pid = -1;   // the TMA box then lies outside the tensor and reads zeros
             }
+          }
+          if (k0 == ta) {
+            if (j == 0) griddep_wait();   // from here on q and the slab are read
+            if (lane == 0) {
+              if (j > 0) ok = mbar_wait(qempty, (j - 1) & 1);
+              if (ok) {
+                mbar_arrive_expect_tx(qfull, nh * D * 2);
+                bulk_load(qbuf, p.q + (static_cast<size_t>(x.b) * p.Hq + head0) * D, nh * D * 2, qfull);
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
           }
           for (int k = k0; k < min(k0 + 32, tz); k += C::NT) {
             const int ntl = min(C::NT, tz - k);
@@ -301,6 +438,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   }
 
   // -------------------------------------------------------------- consumers
+  griddep_wait();
+  zero_empty_units<D>(p, blockIdx.x, ncta, threadIdx.x, C::NCW * 32);
   const int qk_tile = warp % C::NT;
   const int qk_d0 = (warp / C::NT) * C::QK_COLS;
   const int pv_d0 = warp * C::PV_COLS;
@@ -572,52 +711,31 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
           }
         if (warp == 0 && tig == 0)
           reinterpret_cast<float2*>(p.ml_part)[slot * 8 + gid] = make_float2(m_run, l_run);
+        // arrive; the last of the unit's CTAs merges every partial row.  The
+        // barrier orders the CTA's partial writes before thread 0's
+        // release/acquire add, which publishes them and, for the last
+        // arrival, makes the other CTAs' rows visible.
+        named_bar_sync(1, C::NCW * 32);
+        if (threadIdx.x == 0) {
+          const int nct = c_last - c_first + 1;
+          const int old = atom_add_acq_rel_gpu(p.counters + u, 1);
+          int last = 0;
+          if (old == nct - 1) {
+            last = 1;
+            atomicExch(p.counters + u, 0);   // leave the counter zero for the next call
+          } else if (old >= nct) {
+            atomicOr(p.err, FA_DEV_ERR_WORKSPACE);
+          }
+          sh_last = last;
+        }
+        named_bar_sync(1, C::NCW * 32);
+        if (sh_last) merge_unit<D>(p, u, x, nh, head0, c_first, c_last, sx);
       }
     }
     ++j;
     P += x.n;
   }
 consumers_done:;
-}
-
-// Merge the per-CTA partial rows of one (unit, query head) whose tiles were
-// split across CTAs: M = max m_s, l = sum l_s 2^(m_s - M), out = sum o_s 2^(m_s - M) / l.
-template <int D>
-__global__ void __launch_bounds__(D / 4) combine_kernel(const DecK p) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int u = blockIdx.x >> 3, hc = blockIdx.x & 7;
-  const int T = p.ws_hdr[0], ncta = p.ws_hdr[1];
-  if (T == 0) return;
-  const Unit x = unit_of(p, u);
-  const int nh = min(8, p.g - x.c * 8), head0 = x.h * p.g + x.c * 8;
-  if (hc >= nh || x.n == 0) return;
-  const long long P = p.ws_prefix[u];
-  const int cf = cta_of(P, ncta, T), cl = cta_of(P + x.n - 1, ncta, T);
-  if (cf == cl) return;   // finished by its only CTA
-  const int d = threadIdx.x * 4;
-  float M = -INFINITY;
-  for (int c = cf; c <= cl; ++c) M = fmaxf(M, p.ml_part[((static_cast<size_t>(c) + u) * 8 + hc) * 2]);
-  float lsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = cf; c <= cl; ++c) {
-    const size_t row = (static_cast<size_t>(c) + u) * 8 + hc;
-    const float2 v = reinterpret_cast<const float2*>(p.ml_part)[row];
-    const float w = ex2(v.x - M);
-    lsum += v.y * w;
-    const float4 o = *reinterpret_cast<const float4*>(p.o_part + row * D + d);
-    acc.x += o.x * w;
-    acc.y += o.y * w;
-    acc.z += o.z * w;
-    acc.w += o.w * w;
-  }
-  const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(x.b) * p.Hq + head0 + hc) * D + d) = packed;
-  if (p.lse && threadIdx.x == 0)
-    p.lse[static_cast<size_t>(x.b) * p.Hq + head0 + hc] = (M + __log2f(lsum)) * 0.69314718055994531f;
 }
 
 template <int D, int KV>
@@ -628,8 +746,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const DecK& k, cudaStrea
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_kernel<D, KV>, dim3(a.plan.ncta), dim3(C::NTHR), C::SMEM_ALLOC, s, *a.tm_k, *a.tm_v,
                  *a.tm_ks, *a.tm_vs, k);
-  if (e != cudaSuccess || k.ws_hdr == nullptr) return e;
-  return launch_pdl(combine_kernel<D>, dim3(a.plan.units * 8), dim3(D / 4), 0, s, k);
+  return e;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
@@ -641,8 +758,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   k.lse = a.lse;
   if (a.workspace) {
     char* ws = static_cast<char*>(a.workspace);
-    k.ws_hdr = reinterpret_cast<int*>(ws);
-    k.ws_prefix = reinterpret_cast<int*>(ws + a.plan.off_prefix);
+    k.counters = reinterpret_cast<int*>(ws);
     k.ml_part = reinterpret_cast<float*>(ws + a.plan.off_ml);
     k.o_part = reinterpret_cast<float*>(ws + a.plan.off_o);
   }
@@ -661,6 +777,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   k.max_seq_len = a.max_seq_len;
   k.units = a.plan.units;
   k.min_tiles = a.plan.min_tiles;
+  k.early_metadata = a.early_metadata;
   k.scale_log2 = a.sm_scale * 1.4426950408889634f;
   if (a.kv_dtype == FA_KV_INT8) {
     if (a.D == 256) return launch_decode_t<256, 1>(a, k, s);

@@ -43,6 +43,7 @@ struct fa_cache {
   int32_t num_pages = 0;
   int32_t page_size = 0;
   int32_t kv_dtype = FA_KV_BF16;
+  uint32_t flags = 0;   // FA_FLAG_*
 };
 
 namespace fa {
@@ -61,14 +62,15 @@ cudaError_t set_smem_once(const void* fn, int bytes, unsigned int* done_mask);
 // ---------------------------------------------------------------- decode plan
 // The decode kernel splits the concatenated tile lists of all (sequence, KV
 // head, head chunk) units evenly over at most `ncta` CTAs; a unit whose tiles
-// land on one CTA is finished there, the others are merged by a combine pass.
+// land on one CTA is finished there, the others are merged by the last CTA of
+// the unit to finish (an arrival counter per unit lives in the workspace).
 struct DecodePlan {
   int head_chunks = 1;      // ceil(g / 8): query heads are packed 8 per MMA column block
   int units = 0;            // B * Hkv * head_chunks
   int max_tiles = 0;        // 16-row tiles a unit can touch under the length bound
   int min_tiles = 0;        // fewest tiles a CTA is given
   int ncta = 0;             // CTAs launched
-  size_t off_prefix = 0, off_ml = 0, off_o = 0;   // workspace layout (bytes)
+  size_t off_ml = 0, off_o = 0;   // workspace layout (bytes); counters [units] at 0
   size_t ws_bytes = 0;
 };
 DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len);
@@ -100,7 +102,7 @@ struct StoreArgs {
   void* v_slab;
   float* k_scale;
   float* v_scale;
-  int T, Hkv, D, page_size, num_pages, kv_dtype;
+  int T, Hkv, D, page_size, num_pages, kv_dtype, early_metadata;
   unsigned int* err;
 };
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
@@ -119,6 +121,7 @@ struct DecodeArgs {
   const CUtensorMap* tm_ks;
   const CUtensorMap* tm_vs;
   int B, Hq, Hkv, D, kind, window, page_size, num_pages, max_pages_per_seq, max_seq_len, kv_dtype;
+  int early_metadata;
   float sm_scale;
   DecodePlan plan;
   unsigned int* err;

@@ -42,7 +42,7 @@ unsigned int* device_error_word(cudaError_t* err) {
 
 template <int D>
 __global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
-  griddep_wait();
+  if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
     if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
     return;
   }
+  griddep_wait();   // the rows (and the slab) may belong to the previous kernel
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(which ? a.v : a.k) +
                                                     (static_cast<size_t>(t) * a.Hkv + h) * D);
   uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) +
@@ -78,7 +79,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&x)[8]) {
 template <int D>
 __global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
   constexpr int NV = D / 256;            // 16-byte vectors (8 values) per lane
-  griddep_wait();
+  if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
     if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
     return;
   }
+  griddep_wait();   // the rows (and the slab) may belong to the previous kernel
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(which ? a.v : a.k) +
                                                     (static_cast<size_t>(t) * a.Hkv + h) * D);
   float x[NV][8];

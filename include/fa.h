@@ -90,6 +90,7 @@ typedef enum { FA_FULL = 0, FA_SLIDING = 1 } fa_layer_kind;
 #define FA_DEV_ERR_SLOT 0x2u       /* a store slot was >= num_pages * page_size    */
 #define FA_DEV_ERR_BOUND 0x4u      /* a length exceeded the caller's max bound      */
 #define FA_DEV_ERR_TIMEOUT 0x8u    /* a bounded barrier wait ran out                */
+#define FA_DEV_ERR_WORKSPACE 0x10u /* decode workspace counters were not zero      */
 
 /* One attention layer.  kind: fa_layer_kind.  head_dim: 256 or 512 (other
  * widths return FA_ERR_UNSUPPORTED; the pages name exactly these two).
@@ -124,6 +125,22 @@ FA_API fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, 
 
 /* Free the descriptor (NULL is accepted).  Device buffers stay the caller's. */
 FA_API void fa_cache_destroy(fa_cache* cache);
+
+/* Cache flags (fa_cache_set_flags). */
+#define FA_FLAG_EARLY_METADATA 0x1u
+
+/* Set FA_FLAG_* options for every later call on this cache (default 0).
+ * FA_FLAG_EARLY_METADATA: the caller guarantees that the index arrays of each
+ * call (block_table, seq_lens, slot_mapping, qo_indptr, prefix_lens) are
+ * final when the call is enqueued and are not written by the kernel launched
+ * immediately before it on the same stream (the usual case when they are
+ * copied from the host).  The kernels, which launch with programmatic
+ * dependent launch, then read them while that kernel is still finishing, and
+ * wait for it only before touching q, k, v, the slabs and the outputs.
+ * Without the flag every read waits.  Unknown bits: FA_ERR_INVALID_ARG.
+ * No counterpart on the pages: this is a launch-latency option of this
+ * library.  Host only. */
+FA_API fa_status fa_cache_set_flags(fa_cache* cache, uint32_t flags);
 
 /* Slab owner of `layer`: the layer itself if it owns a slab, else its
  * resolved source.  Host only. */
@@ -168,7 +185,9 @@ FA_API fa_status fa_kv_store(fa_cache* cache, int32_t layer, const void* k, cons
                       const int32_t* slot_mapping, int32_t T, void* stream);
 
 /* Workspace bytes fa_paged_decode_attn needs for this layer, batch and bound
- * on the sequence lengths (the split-K partial results).  Host only. */
+ * on the sequence lengths: one arrival counter per (sequence, KV head, group
+ * of up to 8 query heads) followed by the split-K partial rows.  0 when a
+ * single CTA serves the whole call.  Host only. */
 FA_API size_t fa_decode_workspace_bytes(const fa_cache* cache, int32_t layer, int32_t B,
                                  int32_t max_seq_len);
 
@@ -187,8 +206,14 @@ FA_API size_t fa_decode_workspace_bytes(const fa_cache* cache, int32_t layer, in
  * sum-exp of the scaled scores.  seq_lens[b] <= 0 gives out = 0 and
  * lse = -inf.  workspace: device scratch of at least
  * fa_decode_workspace_bytes(cache, layer, B, max_seq_len) bytes (may be NULL
- * when that is 0).  Reference: "unsloth commit dee9371" (shared layers read
- * the source's paged cache on decode) and the regimes above. */
+ * when that is 0), 256-byte aligned.  Zero it once before its first use: its
+ * leading counters must start at zero, and every call that completes leaves
+ * them zero again, so the same buffer serves later calls on the same stream
+ * without clearing.  Calls that run concurrently must not share a workspace.
+ * After a call that reported FA_DEV_ERR_TIMEOUT, zero it again (a counter
+ * found non-zero sets FA_DEV_ERR_WORKSPACE).  Reference: "unsloth commit
+ * dee9371" (shared layers read the source's paged cache on decode) and the
+ * regimes above. */
 FA_API fa_status fa_paged_decode_attn(fa_cache* cache, int32_t layer, const void* q,
                                const int32_t* block_table, int32_t max_pages_per_seq,
                                const int32_t* seq_lens, int32_t B, int32_t max_seq_len,

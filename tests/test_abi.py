@@ -139,3 +139,12 @@ def test_decode_workspace_sizing(fa):
                 per_split = D * 4 + 8
                 assert (ws - 256) <= rows * per_split * ((maxlen + 15) // 16) + 256
     assert c.decode_workspace_bytes(0, 0, 100) == 0
+
+
+def test_cache_flags(fa):
+    c = fa.Cache([lay(FULL, 512, 8, 1)], 8, 16)
+    c.set_flags(fa.FLAG_EARLY_METADATA)
+    c.set_flags(0)
+    with pytest.raises(fa.FAError) as e:
+        c.set_flags(0x80)
+    assert e.value.status == fa.ERR_INVALID_ARG

@@ -157,3 +157,37 @@ def test_int8_decode_full_size():
     lens = case.lens
     seqs = sorted(set(_sample(case.B, 4, 5) + [int(np.argmax(lens))]))
     check_layers(case, seqs)
+
+
+def test_workspace_counters_left_zero_and_reusable():
+    """Split units are merged by their last CTA through arrival counters at the
+    head of the workspace; every call leaves them zero, so one buffer serves
+    consecutive calls (and layers) with identical results."""
+    w = W.e2b_decode()
+    case = DecodeCase(w.layers[:5], W.seq_lens(w)[:32], 16, seed=6)
+    case.store_current()
+    n = max(case.cache.decode_workspace_bytes(i, case.B, case.max_len) for i in range(5))
+    assert n > 0
+    ws = case.fa.workspace(n)
+    first = [case.decode(i, ws=ws) for i in range(5)]
+    units = case.B * 1   # one KV head, 8 query heads: one unit per sequence
+    assert int(ws[: units * 4].count_nonzero()) == 0
+    again = [case.decode(i, ws=ws) for i in range(5)]
+    for (a, la), (b, lb) in zip(first, again):
+        assert torch.equal(a, b) and torch.equal(la, lb)
+    assert case.fa.device_error() == 0
+
+
+def test_early_metadata_flag_gives_identical_results():
+    """Reading the index arrays before the preceding kernel finishes changes
+    only when they are read, never what is computed."""
+    w = W.e2b_decode()
+    case = DecodeCase(w.layers, W.seq_lens(w)[:24], 16, seed=8)
+    case.store_current()
+    plain = [case.decode(i) for i in range(len(case.layers))]
+    case.cache.set_flags(case.fa.FLAG_EARLY_METADATA)
+    case.store_current()
+    early = [case.decode(i) for i in range(len(case.layers))]
+    for (a, la), (b, lb) in zip(plain, early):
+        assert torch.equal(a, b) and torch.equal(la, lb)
+    assert case.fa.device_error() == 0
