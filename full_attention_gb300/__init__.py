@@ -22,6 +22,8 @@ DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE = 
 
 FLAG_EARLY_METADATA = 1
 
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NOT_BOUND, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4, 5
 
 
@@ -53,6 +55,7 @@ def _load() -> ctypes.CDLL:
         "fa_kv_store": (i32, [vp, i32, vp, vp, vp, i32, vp]),
         "fa_decode_workspace_bytes": (sz, [vp, i32, i32, i32]),
         "fa_paged_decode_attn": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
+        "fa_paged_decode_attn_noalloc": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
         "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
         "fa_get_device_error": (i32, [ctypes.POINTER(i32), vp]),
         "fa_last_error": (ctypes.c_char_p, []),
@@ -174,6 +177,14 @@ class Cache:
         _check(_lib.fa_paged_decode_attn(self._h, layer, _p(q), _p(block_table), int(block_table.shape[1]),
                                          _p(seq_lens), int(q.shape[0]), int(max_seq_len), _p(out), _p(lse),
                                          _p(workspace), ws_bytes, _s(stream)))
+
+    def decode_noalloc(self, layer: int, q, block_table, seq_lens, max_seq_len: int, out, lse=None,
+                       stream=None) -> None:
+        """fa_paged_decode_attn_noalloc: decode with the library's fixed scratch
+        (no device allocation); calls must not overlap on the GPU."""
+        _check(_lib.fa_paged_decode_attn_noalloc(self._h, layer, _p(q), _p(block_table), int(block_table.shape[1]),
+                                                 _p(seq_lens), int(q.shape[0]), int(max_seq_len), _p(out), _p(lse),
+                                                 _s(stream)))
 
     def extend(self, layer: int, q, k_ext, v_ext, qo_indptr, prefix_lens, block_table, max_q_len: int,
                max_prefix_len: int, out, lse=None, stream=None) -> None:

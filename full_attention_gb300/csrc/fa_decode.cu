@@ -33,6 +33,7 @@
 // the V scale is folded into P (normalised by the step's largest scale, which
 // joins the running rescale), and the MMAs run in fp16.
 #include <cfloat>
+#include <mutex>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -787,4 +788,66 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   return launch_decode_t<512, 0>(a, k, s);
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free decode: the same kernel with its scratch in a file-scope
+// device array of FA_NOALLOC_SCRATCH_BYTES, for callers that cannot allocate
+// device memory.  The array is part of the loaded module, so every GPU that
+// loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, never a device address, so
+// the address is looked up once per device (with that device current).
+static void* noalloc_scratch(cudaError_t* err) {
+  static std::mutex mu;
+  static void* ptrs[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  *err = cudaSuccess;
+  return ptrs[dev];
+}
+
 }  // namespace fa
+
+extern "C" fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, const void* q,
+                                                  const int32_t* block_table, int32_t max_pages_per_seq,
+                                                  const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                                  void* out, float* lse, void* stream) {
+  if (!cache || layer < 0 || layer >= static_cast<int32_t>(cache->layers.size()))
+    return fa::fail(FA_ERR_INVALID_ARG, "cache is NULL or layer %d out of range", layer);
+  if (B <= 0 || max_seq_len <= 0)   // let the regular entry point validate and report
+    return fa_paged_decode_attn(cache, layer, q, block_table, max_pages_per_seq, seq_lens, B, max_seq_len, out,
+                                lse, nullptr, 0, stream);
+  const fa::DecodePlan plan = fa::plan_decode(cache, layer, B, max_seq_len);
+  if (plan.ws_bytes > FA_NOALLOC_SCRATCH_BYTES)
+    return fa::fail(FA_ERR_WORKSPACE,
+                    "allocation-free decode needs %zu bytes of scratch for B=%d, max_seq_len=%d; its fixed "
+                    "scratch holds %zu bytes (use fa_paged_decode_attn with a caller workspace)",
+                    plan.ws_bytes, B, max_seq_len, static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES));
+  void* ws = nullptr;
+  if (plan.ws_bytes) {
+    cudaError_t ce;
+    ws = fa::noalloc_scratch(&ce);
+    if (!ws) return fa::fail(FA_ERR_CUDA, "scratch address lookup: %s", cudaGetErrorString(ce));
+    // the arrival counters must start at zero whatever an earlier call left
+    ce = cudaMemsetAsync(ws, 0, plan.off_ml, static_cast<cudaStream_t>(stream));
+    if (ce != cudaSuccess) return fa::fail(FA_ERR_CUDA, "clearing scratch counters: %s", cudaGetErrorString(ce));
+  }
+  return fa_paged_decode_attn(cache, layer, q, block_table, max_pages_per_seq, seq_lens, B, max_seq_len, out, lse,
+                              ws, plan.ws_bytes, stream);
+}

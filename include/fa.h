@@ -220,6 +220,34 @@ FA_API fa_status fa_paged_decode_attn(fa_cache* cache, int32_t layer, const void
                                void* out, float* lse, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Largest scratch the allocation-free decode below can use (bytes). */
+#define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Allocation-free paged decode attention.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory, such as
+ * a plugin inside a serving framework that hands out no allocator, or an
+ * engine that reserves its whole memory budget at start-up and forbids
+ * cudaMalloc afterwards (it can block or synchronise the device on the hot
+ * path).  It computes exactly what fa_paged_decode_attn computes, with the
+ * same arguments minus the workspace: its scratch is a fixed array of
+ * FA_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library keeps until the process exits.
+ * - Limit: a call whose fa_decode_workspace_bytes(cache, layer, B,
+ *   max_seq_len) exceeds FA_NOALLOC_SCRATCH_BYTES returns FA_ERR_WORKSPACE and
+ *   launches nothing (8 MiB covers, e.g., a batch of 128 at head_dim 512).
+ * - Set-up: the first call on each device looks up the array's device address
+ *   (with that device current); make that first call before any CUDA-graph
+ *   stream capture.
+ * - Sharing: every call uses the same array.  Each call clears the counters
+ *   it needs before launching, but calls whose work overlaps on the GPU
+ *   (different streams, or different threads without ordering) race on the
+ *   array and produce wrong results; serialise them.
+ * - No cudaMalloc, cudaFree or other allocating routine is called. */
+FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, const void* q,
+                                             const int32_t* block_table, int32_t max_pages_per_seq,
+                                             const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                                             void* out, float* lse, void* stream);
+
 /* Chunked-prefill / extend attention ("FreeToken PR #898", description: the
  * extend kernel takes the prefix from the slab and the current chunk from
  * k_extend / v_extend; "pegainfer issue #807": the prefill chunk size is a
