@@ -56,7 +56,7 @@ def _load() -> ctypes.CDLL:
         "fa_decode_workspace_bytes": (sz, [vp, i32, i32, i32]),
         "fa_paged_decode_attn": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_attn_noalloc": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
-        "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
+        "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "fa_get_device_error": (i32, [ctypes.POINTER(i32), vp]),
         "fa_last_error": (ctypes.c_char_p, []),
         "fa_status_string": (ctypes.c_char_p, [i32]),
@@ -191,7 +191,8 @@ class Cache:
         maxp = int(block_table.shape[1]) if block_table is not None else 0
         _check(_lib.fa_paged_extend_attn(self._h, layer, _p(q), _p(k_ext), _p(v_ext), _p(qo_indptr),
                                          _p(prefix_lens), _p(block_table), maxp, int(prefix_lens.numel()),
-                                         int(max_q_len), int(max_prefix_len), _p(out), _p(lse), _s(stream)))
+                                         int(q.shape[0]), int(max_q_len), int(max_prefix_len), _p(out), _p(lse),
+                                         _s(stream)))
 
 
 def device_error(stream=None) -> int:

@@ -124,6 +124,38 @@ static fa_status encode_slab_map(CUtensorMap* tm, void* base, int D, int kv_dtyp
   return FA_OK;
 }
 
+// Queries q [N][Hq][D] as 4-D (64-column block elements, head, token, block
+// index): a box (64, g, 128/g, 1) lands as 128 rows ordered (token, head) x 128 B.
+static fa_status encode_q_map(CUtensorMap* tm, const void* q, int N, int Hq, int D, int g) {
+  auto enc = get_encoder();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(D / 64)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2, 128};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(128 / g), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (CUresult %d)", (int)r);
+  return FA_OK;
+}
+
+// Chunk rows k_ext / v_ext [N][Hkv][D] as 4-D (64 elements, block, KV head,
+// token): a box (64, 1, 1, 64) lands as 64 token rows x 128 B.
+static fa_status encode_ext_map(CUtensorMap* tm, const void* x, int N, int Hkv, int D) {
+  auto enc = get_encoder();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(D / 64), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
+  cuuint32_t box[4] = {64, 1, 1, 64};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (k/v chunk) failed (CUresult %d)", (int)r);
+  return FA_OK;
+}
+
 // 2-D map over fp32 scales [rows]: dim0 = 16 scales of one tile, dim1 = tile.
 static fa_status encode_scale_map(CUtensorMap* tm, float* base, uint64_t rows) {
   auto enc = get_encoder();
@@ -419,13 +451,18 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
 
 fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const void* k_ext, const void* v_ext,
                                const int32_t* qo_indptr, const int32_t* prefix_lens, const int32_t* block_table,
-                               int32_t max_pages_per_seq, int32_t B, int32_t max_q_len, int32_t max_prefix_len,
-                               void* out, float* lse, void* stream) {
+                               int32_t max_pages_per_seq, int32_t B, int32_t num_tokens, int32_t max_q_len,
+                               int32_t max_prefix_len, void* out, float* lse, void* stream) {
   fa_status st = check_layer(c, layer);
   if (st) return st;
-  if (B < 0 || max_q_len < 0 || max_prefix_len < 0) return fail(FA_ERR_INVALID_ARG, "negative size");
-  if (B == 0 || max_q_len == 0) return ok();
+  if (B < 0 || max_q_len < 0 || max_prefix_len < 0 || num_tokens < 0) return fail(FA_ERR_INVALID_ARG, "negative size");
+  if (B == 0 || max_q_len == 0 || num_tokens == 0) return ok();
   const Layer& L = c->layers[layer];
+  const int g = L.d.num_q_heads / L.d.num_kv_heads;
+  if (128 % g != 0)
+    return fail(FA_ERR_UNSUPPORTED, "extend packs Hq/Hkv = %d query heads into 128-row tiles; it must divide 128", g);
+  if (c->kv_dtype != FA_KV_BF16)
+    return fail(FA_ERR_UNSUPPORTED, "extend over the int8 per-token-head format is not built");
   const Slab* s = nullptr;
   if ((st = check_bound(c, layer, &s))) return st;
   if (!q || !k_ext || !v_ext || !qo_indptr || !prefix_lens || !out || (max_prefix_len > 0 && !block_table))
@@ -467,8 +504,13 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.max_q_len = max_q_len;
   a.max_prefix_len = max_prefix_len;
   a.kv_dtype = c->kv_dtype;
+  a.num_tokens = num_tokens;
+  a.early_metadata = (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0;
   a.sm_scale = L.d.sm_scale;
   a.err = err;
+  if ((st = encode_q_map(&a.tm_q, q, num_tokens, L.d.num_q_heads, L.d.head_dim, g))) return st;
+  if ((st = encode_ext_map(&a.tm_kx, k_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
+  if ((st = encode_ext_map(&a.tm_vx, v_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
   ce = launch_extend(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "extend launch: %s", cudaGetErrorString(ce));
   return ok();

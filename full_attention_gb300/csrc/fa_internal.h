@@ -146,9 +146,12 @@ struct ExtendArgs {
   void* out;
   float* lse;
   int B, Hq, Hkv, D, kind, window, page_size, num_pages, max_pages_per_seq, max_q_len,
-      max_prefix_len, kv_dtype;
+      max_prefix_len, kv_dtype, num_tokens, early_metadata;
   float sm_scale;
   unsigned int* err;
+  // per-call maps: q as (64-column block, head, token, block index) boxes of
+  // (64, g, 128/g, 1); k_ext / v_ext as (64, block, KV head, token) boxes of (64, 1, 1, 64)
+  CUtensorMap tm_q, tm_kx, tm_vx;
 };
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s);
 

@@ -258,16 +258,21 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * v_ext, bf16, never quantised), under the layer's mask.
  * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
  * (for a shared layer: the source layer's current k, v).  qo_indptr: int32
- * [B+1], non-decreasing, qo_indptr[0] = 0.  prefix_lens: int32 [B].
+ * [B+1], non-decreasing, qo_indptr[0] = 0.  num_tokens: the rows of q, k_ext,
+ * v_ext and out (qo_indptr[B]; the kernels never read past it).
+ * prefix_lens: int32 [B].
  * max_q_len >= every n_b, max_prefix_len >= every P_b (longer ones set
  * FA_DEV_ERR_BOUND and are cut).  out: bf16 [N][Hq][D]; lse: optional float
  * [N][Hq].  The chunk's own k, v are read from k_ext / v_ext even if they
- * were stored first. */
+ * were stored first.  Hq / Hkv must divide 128 (query heads of a KV head are
+ * packed into 128-row tensor-core tiles) and the format must be bf16; other
+ * cases return FA_ERR_UNSUPPORTED. */
 FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void* q, const void* k_ext,
                                const void* v_ext, const int32_t* qo_indptr,
                                const int32_t* prefix_lens, const int32_t* block_table,
-                               int32_t max_pages_per_seq, int32_t B, int32_t max_q_len,
-                               int32_t max_prefix_len, void* out, float* lse, void* stream);
+                               int32_t max_pages_per_seq, int32_t B, int32_t num_tokens,
+                               int32_t max_q_len, int32_t max_prefix_len, void* out, float* lse,
+                               void* stream);
 
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device (FA_DEV_ERR_* bits; 0 = no error). */
