@@ -415,9 +415,147 @@ def e2e_decode(step, args, torch):
             "d2h_bytes_per_step": int(bo), "ms_per_step": round(t * 1e3, 4), "path": "eager C-ABI calls"}
 
 
+def visible_pairs(kind, window, P, n):
+    """(query, key) pairs a chunk of n tokens over a prefix of P sees."""
+    tot = 0
+    for i in range(n):
+        q = P + i
+        tot += min(window, q + 1) if kind == W.SLIDING else q + 1
+    return tot
+
+
+class PrefillStep:
+    """The chunked-prefill workload: B prompts of S tokens in chunks of C; per
+    chunk and owning layer, the KV store of the chunk rows then extend."""
+
+    def __init__(self, w: W.ExtendWorkload, device):
+        import torch
+        import full_attention_gb300 as fa
+        self.torch, self.fa, self.w, self.device = torch, fa, w, device
+        B, S, C = w.batch, w.prompt_len, w.chunk
+        self.nchunks = S // C
+        lens = np.full(B, S, np.int32)
+        plan = W.plan_pages(lens, w.page_size, w.seed)
+        self.cache = fa.Cache(w.layers, plan.num_pages, w.page_size, w.kv_dtype)
+        self.cache.set_flags(fa.FLAG_EARLY_METADATA)
+        self.slabs = self.cache.allocate(device)
+        for k, v, _, _ in self.slabs.values():
+            k.zero_()
+            v.zero_()
+        self.bt = torch.from_numpy(plan.block_table).to(device)
+        self.indptr = torch.arange(0, B * C + 1, C, dtype=torch.int32, device=device)
+        self.inputs = []      # [chunk][layer] -> (q, k, v, slots)
+        self.prefix = []
+        self.flops = []       # [chunk][layer]
+        for c in range(self.nchunks):
+            P = c * C
+            self.prefix.append(torch.full((B,), P, dtype=torch.int32, device=device))
+            pos = np.arange(P, P + C)
+            slots = np.concatenate([W.slots_for_positions(plan.block_table[b], pos, w.page_size) for b in range(B)])
+            row, fl = [], []
+            for li, d in enumerate(w.layers):
+                s0 = w.seed * 1000 + 10 * c + 3 * li
+                q = W.randn_bf16((B * C, d["num_q_heads"], d["head_dim"]), s0, device)
+                k = W.randn_bf16((B * C, d["num_kv_heads"], d["head_dim"]), s0 + 1, device)
+                v = W.randn_bf16((B * C, d["num_kv_heads"], d["head_dim"]), s0 + 2, device)
+                row.append((q, k, v, torch.from_numpy(slots).to(device)))
+                fl.append(4.0 * d["head_dim"] * d["num_q_heads"] * B *
+                          visible_pairs(d["kind"], d["window"], P, C))
+            self.inputs.append(row)
+            self.flops.append(fl)
+        self.out = [torch.empty((B * C, d["num_q_heads"], d["head_dim"]), dtype=torch.bfloat16, device=device)
+                    for d in w.layers]
+        self.total_flops = sum(sum(f) for f in self.flops)
+        self.tokens = B * S
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return self.nchunks * len(self.w.layers) * 2
+
+    def run(self, events=None):
+        C = self.w.chunk
+        for c in range(self.nchunks):
+            for li in range(len(self.w.layers)):
+                q, k, v, slots = self.inputs[c][li]
+                self.cache.store(li, k, v, slots)
+                if events is not None:
+                    events[c][li][0].record()
+                self.cache.extend(li, q, k, v, self.indptr, self.prefix[c], self.bt, C, self.nchunks * C, self.out[li])
+                if events is not None:
+                    events[c][li][1].record()
+
+
 def prefill_measure(args, dev):
     """Chunked prefill TFLOP/s on the chunked-prefill workload (extend kernel)."""
-    return {"status": "extend kernel not built yet"}
+    import torch
+    import full_attention_gb300 as fa
+    w = W.chunked_prefill()
+    step = PrefillStep(w, dev)
+    for _ in range(3):
+        step.run()
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    nl = len(w.layers)
+    events = [[(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nl)] for _ in range(step.nchunks)]
+
+    def capture(ev):
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                step.run(ev)
+            torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step.run(ev)
+            torch.cuda.synchronize()
+            return g
+        except Exception as e:
+            print(f"# prefill graph capture failed ({e})", file=sys.stderr)
+            torch.cuda.synchronize()
+            return None
+
+    g_plain, g_ev = capture(None), capture(events)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(3, min(args.prefill_steps, 50))
+    tot = 0.0
+    for _ in range(reps):
+        flush.zero_()
+        e0.record()
+        g_plain.replay() if g_plain is not None else step.run()
+        e1.record()
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    t = tot / reps / 1e3
+    ext_ms = [[0.0] * nl for _ in range(step.nchunks)]
+    for _ in range(reps):
+        flush.zero_()
+        g_ev.replay() if g_ev is not None else step.run(events)
+        torch.cuda.synchronize()
+        for c in range(step.nchunks):
+            for li in range(nl):
+                ext_ms[c][li] += events[c][li][0].elapsed_time(events[c][li][1]) / reps
+    assert fa.device_error() == 0
+    _, bf16, bf16s, src = measured_peaks()
+    ext_t = sum(sum(r) for r in ext_ms) / 1e3
+    per_layer = {}
+    for li, d in enumerate(w.layers):
+        fl = sum(step.flops[c][li] for c in range(step.nchunks))
+        tl = sum(ext_ms[c][li] for c in range(step.nchunks)) / 1e3
+        per_layer["sliding D256" if d["kind"] == W.SLIDING else "full D512"] = {
+            "tflops": round(fl / tl / 1e12, 1), "ms": round(tl * 1e3, 4),
+            "executed_flop_factor": 1.5 if d["head_dim"] == 512 else 1.0}
+    achieved = step.total_flops / ext_t / 1e12
+    return {"workload": w.name, "value": round(step.total_flops / t / 1e12, 1), "unit": "TFLOP/s",
+            "ms_per_prefill": round(t * 1e3, 4), "tokens_per_s": round(step.tokens / t, 1),
+            "algorithmic_tflop": round(step.total_flops / 1e12, 4),
+            "roofline": {"kernel": "extend_kernel (tcgen05 chunked prefill)", "bound": "tensor",
+                         "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
+                         "frac": round(achieved / bf16, 3), "peak_source": src + " (dense bf16 burst)",
+                         "traffic": None, "per_layer": per_layer},
+            "gpu_launches_per_prefill": step.launches(), "graph": g_plain is not None}
 
 
 # ----------------------------------------------------------------------------
@@ -570,6 +708,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--prefill-steps", type=int, default=20)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
