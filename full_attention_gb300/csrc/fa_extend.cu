@@ -39,22 +39,21 @@ struct ExtCfg {
   static constexpr int DS = 256;                // output columns per CTA
   static constexpr int KB = D / 64;             // 64-column blocks of head_dim
   static constexpr int Q_BYTES = M * D * 2;     // [KB][128][64] bf16
-  static constexpr int KCH_BYTES = NK * 64 * 2; // one K chunk: 64 keys x 64 columns
-  static constexpr int KSTAGES = 4;
-  static constexpr int V_BYTES = NK * DS * 2;   // [4 blocks][64 keys][64 columns]
-  static constexpr int VSTAGES = 2;
-  static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_V = OFF_K + KSTAGES * KCH_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VSTAGES * V_BYTES;
-  // barriers: q_full, k_full[4], k_empty[4], v_full[2], v_empty[2], s_full[2], p_full[2], o_bar[2]
-  static constexpr int NBAR = 1 + 2 * KSTAGES + 2 * VSTAGES + 2 + 2 + 2;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int SLOT = NK * 64 * 2;      // one ring slot: 64 keys x 64 columns (a K chunk or a V block)
+  static constexpr int BAR_BYTES = 512;
+  // the rest of shared memory is a ring of slots; per tile KB K chunks and 4 V blocks pass through it
+  static constexpr int NSLOT = (232448 - 1024 - Q_BYTES - BAR_BYTES) / SLOT;
+  static constexpr int OFF_RING = Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   static constexpr int NTHR = 6 * 32;
   // tensor memory columns: O [0, 256), S/P buffers [256, 320) and [320, 384)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 256;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static_assert((1 + 2 * NSLOT + 2 + 2 + 2) * 8 <= BAR_BYTES, "barrier space");
+  static_assert(NSLOT >= KB + 4, "a ring must hold one tile");
 };
 
 struct ExtK {
@@ -117,18 +116,15 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem;
-  uint8_t* kring = smem + C::OFF_K;
-  uint8_t* vring = smem + C::OFF_V;
+  uint8_t* ring = smem + C::OFF_RING;
   uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* k_full = q_full + 1;
-  uint64_t* k_empty = k_full + C::KSTAGES;
-  uint64_t* v_full = k_empty + C::KSTAGES;
-  uint64_t* v_empty = v_full + C::VSTAGES;
-  uint64_t* s_full = v_empty + C::VSTAGES;
+  uint64_t* full = q_full + 1;          // [NSLOT]
+  uint64_t* empty = full + C::NSLOT;    // [NSLOT]
+  uint64_t* s_full = empty + C::NSLOT;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_bar = p_full + 2;
   __shared__ uint32_t tmem_slot;
-  __shared__ uint64_t done_bar;
+  __shared__ uint64_t done_bar, san_bar;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!p.early_metadata) griddep_wait();
@@ -139,13 +135,9 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < C::KSTAGES; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < C::VSTAGES; ++i) {
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -154,6 +146,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     mbar_init(&o_bar[0], 1);
     mbar_init(&o_bar[1], 1);
     mbar_init(&done_bar, 1);
+    mbar_init(&san_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
@@ -165,8 +158,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Emission order = the MMA issuer's consumption order: K_0, then for each
+    // t >= 1: K_t (if any) and V_{t-1}.  Page ids are loaded a tile ahead.
     const uint64_t pol = l2_policy_evict_last();   // K/V tiles are shared by the CTAs of a (sequence, head)
-    int kc = 0, vc = 0;
+    int e = 0;
     bool ok = true;
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -175,12 +170,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         tma_load_4d(qs + kb * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
     }
     const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
-    for (int j = 0; ok && j < nt; ++j) {
-      const int st0 = x.start(j);
-      const bool pre = x.prefix(j);
+    auto load_pid = [&](int j) -> int {   // lanes 0-3: page of 16-row box `lane` of tile j
       int pid = -1;
-      if (pre && lane < 4) {
-        const int pos = st0 + 16 * lane;
+      if (j < nt && x.prefix(j) && lane < 4) {
+        const int pos = x.start(j) + 16 * lane;
         if (pos < x.P) {
           pid = __ldg(bt + pos / p.page_size);
           if (pid < 0 || pid >= p.num_pages) {
@@ -189,104 +182,128 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
           }
         }
       }
-      int row0[4];
+      return pid;
+    };
+    auto rows_of = [&](int j, int pid, int (&row0)[4]) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int pg = __shfl_sync(0xffffffffu, pid, i);
-        row0[i] = (pg * p.Hkv + x.h) * p.page_size + ((st0 + 16 * i) % p.page_size);
+        row0[i] = (pg * p.Hkv + x.h) * p.page_size + ((x.start(j) + 16 * i) % p.page_size);
       }
-      const int xrow = x.qo0 + (st0 - x.P);   // chunk tiles: first token row in k_ext / v_ext
-      if (lane == 0) {
-        for (int kb = 0; ok && kb < C::KB; ++kb, ++kc) {
-          const int st = kc % C::KSTAGES;
-          ok = mbar_wait(&k_empty[st], ((kc / C::KSTAGES) & 1) ^ 1);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&k_full[st], C::KCH_BYTES);
-          uint8_t* dst = kring + st * C::KCH_BYTES;
-          if (pre) {
+    };
+    // one ring slot: wait for it to be free, then fill it with a K chunk or V block
+    auto emit = [&](int j, int blk, bool is_v, const int (&row0)[4]) {
+      const int sl = e % C::NSLOT;
+      ok = ok && mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+      if (!ok) return;
+      mbar_arrive_expect_tx(&full[sl], C::SLOT);
+      uint8_t* dst = ring + sl * C::SLOT;
+      const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+      if (x.prefix(j)) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tma_load_3d(dst + i * 2048, &tm_k, &k_full[st], 0, kb, row0[i], pol);
-          } else {
-            tma_load_4d(dst, &tm_kx, &k_full[st], 0, kb, x.h, xrow, pol);
-          }
-        }
-        if (ok) {
-          const int vs = vc % C::VSTAGES;
-          ok = mbar_wait(&v_empty[vs], ((vc / C::VSTAGES) & 1) ^ 1);
-          if (ok) {
-            mbar_arrive_expect_tx(&v_full[vs], C::V_BYTES);
-            uint8_t* dst = vring + vs * C::V_BYTES;
-#pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-              const int blk = x.ds * 4 + i4;
-              if (pre) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  tma_load_3d(dst + i4 * 8192 + i * 2048, &tm_v, &v_full[vs], 0, blk, row0[i], pol);
-              } else {
-                tma_load_4d(dst + i4 * 8192, &tm_vx, &v_full[vs], 0, blk, x.h, xrow, pol);
-              }
-            }
-            ++vc;
-          }
-        }
+        for (int i = 0; i < 4; ++i) tma_load_3d(dst + i * 2048, tm, &full[sl], 0, blk, row0[i], pol);
+      } else {
+        tma_load_4d(dst, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, x.qo0 + (x.start(j) - x.P), pol);
       }
+      ++e;
+    };
+    int pid_next = load_pid(0);
+    int row_cur[4], row_prev[4];
+    for (int t = 0; ok && t <= nt; ++t) {
+      if (t < nt) {
+        const int pid = pid_next;
+        pid_next = load_pid(t + 1);
+        rows_of(t, pid, row_cur);
+        if (lane == 0)
+          for (int kb = 0; ok && kb < C::KB; ++kb) emit(t, kb, false, row_cur);
+      }
+      if (t >= 1 && lane == 0)
+        for (int i4 = 0; ok && i4 < 4; ++i4) emit(t - 1, x.ds * 4 + i4, true, row_prev);
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int jb = t - 1;
+      if (ok && t >= 1 && x.prefix(jb) && x.start(jb) + 64 > x.P && (x.P & 15) != 0) {
+        // The last prefix page's slots at positions >= P hold whatever they held
+        // before (their P is 0, but NaN * 0 is NaN in the MMA): wait for this
+        // tile's V blocks to land and zero those rows, then release the softmax.
+        const int e_last = __shfl_sync(0xffffffffu, e, 0);
+        const int r0 = x.P - x.start(jb), r1 = min(64, ((x.P + 15) & ~15) - x.start(jb));
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const int idx = e_last - 4 + i4, sl = idx % C::NSLOT;
+          bool landed = true;
+          if (lane == 0) landed = mbar_wait(&full[sl], (idx / C::NSLOT) & 1);
+          ok = __shfl_sync(0xffffffffu, landed, 0) && ok;
+          if (!ok) break;
+          uint8_t* vt = ring + sl * C::SLOT;
+          for (int u = lane; u < (r1 - r0) * 8; u += 32)
+            *reinterpret_cast<uint4*>(vt + sw128(r0 + u / 8, u % 8)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(&san_bar);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) row_prev[i] = row_cur[i];
     }
     if (lane == 0) {
       if (!ok) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
       // drain: no bulk copy may still be landing when the CTA exits
       if (!mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-      for (int i = max(0, kc - C::KSTAGES); i < kc; ++i)
-        if (!mbar_wait(&k_full[i % C::KSTAGES], (i / C::KSTAGES) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-      for (int i = max(0, vc - C::VSTAGES); i < vc; ++i)
-        if (!mbar_wait(&v_full[i % C::VSTAGES], (i / C::VSTAGES) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+      for (int i = max(0, e - C::NSLOT); i < e; ++i)
+        if (!mbar_wait(&full[i % C::NSLOT], (i / C::NSLOT) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);
-      const uint32_t idO = umma_idesc_bf16(C::M, C::DS, true);
+      const uint32_t idO = umma_idesc_bf16(C::M, 64, true);
       bool ok = mbar_wait(q_full, 0);
-      int kc = 0;
-      auto pv = [&](int i) {
-        const int sb = i & 1, vs = i % C::VSTAGES;
-        ok = ok && mbar_wait(&p_full[sb], (i >> 1) & 1);
-        ok = ok && mbar_wait(&v_full[vs], (i / C::VSTAGES) & 1);
-        if (!ok) return;
+      int e = 0;
+      auto take = [&]() -> uint32_t {   // wait for the next ring slot, return its address
+        const int sl = e % C::NSLOT;
+        ok = ok && mbar_wait(&full[sl], (e / C::NSLOT) & 1);
         tc_fence_after();
-        const uint32_t vbase = smem_u32(vring + vs * C::V_BYTES);
-#pragma unroll
-        for (int ks = 0; ks < C::NK / 16; ++ks)
-          umma_ts(tmem, tmem + C::S_COL0 + sb * 64 + ks * 8, umma_desc_sw128(vbase + ks * 2048, 8192, 1024), idO,
-                  (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&v_empty[vs]);
-        umma_commit(&o_bar[i & 1]);   // PV i completes phase i / 2 of o_bar[i & 1]
+        return smem_u32(ring + sl * C::SLOT);
       };
-      for (int j = 0; ok && j < nt; ++j) {
-        const int sb = j & 1;
-        if (j >= 2) ok = mbar_wait(&o_bar[j & 1], ((j - 2) >> 1) & 1);   // PV_{j-2} has read P from this buffer
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t s_tmem = tmem + C::S_COL0 + sb * 64;
-        for (int kb = 0; kb < C::KB; ++kb, ++kc) {
-          const int st = kc % C::KSTAGES;
-          ok = mbar_wait(&k_full[st], (kc / C::KSTAGES) & 1);
+      auto give = [&]() {   // release the slot once the MMAs reading it complete
+        umma_commit(&empty[e % C::NSLOT]);
+        ++e;
+      };
+      for (int t = 0; ok && t <= nt; ++t) {
+        if (t < nt) {
+          const int sb = t & 1;
+          if (t >= 2) ok = mbar_wait(&o_bar[t & 1], ((t - 2) >> 1) & 1);   // PV_{t-2} has read P from this buffer
+          tc_fence_after();
+          const uint32_t s_tmem = tmem + C::S_COL0 + sb * 64;
+          for (int kb = 0; ok && kb < C::KB; ++kb) {
+            const uint32_t kbase = take();
+            if (!ok) break;
+            const uint32_t qb = smem_u32(qs + kb * (C::M * 128));
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024),
+                      idS, (kb > 0 || ks > 0) ? 1u : 0u);
+            give();
+          }
+          if (!ok) break;
+          umma_commit(&s_full[sb]);
+        }
+        if (t >= 1) {
+          const int i = t - 1, sb = i & 1;
+          ok = ok && mbar_wait(&p_full[sb], (i >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qb = smem_u32(qs + kb * (C::M * 128));
-          const uint32_t kbase = smem_u32(kring + st * C::KCH_BYTES);
+          for (int i4 = 0; ok && i4 < 4; ++i4) {
+            const uint32_t vbase = take();   // V block i4: 64 keys x 64 output columns, MN-major
+            if (!ok) break;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024), idS,
-                    (kb > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&k_empty[st]);
+            for (int ks = 0; ks < C::NK / 16; ++ks)
+              umma_ts(tmem + i4 * 64, tmem + C::S_COL0 + sb * 64 + ks * 8,
+                      umma_desc_sw128(vbase + ks * 2048, 8192, 1024), idO, (i > 0 || ks > 0) ? 1u : 0u);
+            give();
+          }
+          umma_commit(&o_bar[i & 1]);   // PV i completes phase i / 2 of o_bar[i & 1]
         }
-        if (!ok) break;
-        umma_commit(&s_full[sb]);
-        if (j >= 1) pv(j - 1);
       }
-      if (ok && nt >= 1) pv(nt - 1);
       if (!ok) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
       // every MMA this thread issued has finished before tensor memory is freed
       umma_commit(&done_bar);
@@ -317,13 +334,24 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       const bool pre = x.prefix(j);
       float sv[64];
       float mt = -INFINITY;
+      // this row's visible keys in this tile are the columns [clo, chi]: one
+      // interval per row (causal, window, prefix end), two compares per key
+      const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
+      const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.P - 1) : qpos);
+      const int clo = klo - st0, chi = khi - st0;
+      const float sc = p.scale_log2;
+      if (__all_sync(0xffffffffu, clo <= 0 && chi >= 63)) {   // the whole tile is visible to the warp's rows
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int kp = st0 + c;
-        bool v = row_ok && kp <= qpos && (p.kind == FA_FULL || qpos - kp < p.window);
-        if (pre) v = v && kp < x.P;
-        sv[c] = v ? __uint_as_float(sr[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, sv[c]);
+        for (int c = 0; c < 64; ++c) {
+          sv[c] = __uint_as_float(sr[c >> 5][c & 31]) * sc;
+          mt = fmaxf(mt, sv[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sr[c >> 5][c & 31]) * sc : -INFINITY;
+          mt = fmaxf(mt, sv[c]);
+        }
       }
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + 8.0f;   // rescale only when the max grows by more than 2^8
@@ -361,21 +389,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       tmem_st32(trow + s_col, pk);
       tmem_st_wait();
       if (pre && st0 + 64 > x.P && (x.P & 15) != 0) {
-        // the slab rows of the last prefix page past P hold whatever the slots
-        // held before; their P is 0, but zero them so no NaN enters the MMA
-        // (each warp zeroes its share and fences before arriving on p_full,
-        // which the MMA issuer waits for before reading V)
-        const int vs = j % C::VSTAGES;
-        ok = mbar_wait(&v_full[vs], (j / C::VSTAGES) & 1);
+        // the producer zeroes the stale slab rows of the last prefix page
+        // (positions P .. next multiple of 16) in V_j before the PV MMA reads them
+        ok = mbar_wait(&san_bar, 0);
         if (__any_sync(0xffffffffu, !ok)) break;
-        const int r0 = x.P - st0, r1 = min(64, ((x.P + 15) & ~15) - st0);
-        uint8_t* vt = vring + vs * C::V_BYTES;
-        const int units = (r1 - r0) * 4 * 8;   // rows x blocks x 16-byte units
-        for (int e = threadIdx.x - 64; e < units; e += 128) {
-          const int rr = r0 + e / 32, blk = (e / 8) % 4, u = e % 8;
-          *reinterpret_cast<uint4*>(vt + blk * 8192 + sw128(rr, u)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
       }
       tc_fence_before();
       __syncwarp();
