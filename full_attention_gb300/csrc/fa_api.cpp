@@ -420,6 +420,8 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.q = q;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
+  a.k = s->k;
+  a.v = s->v;
   a.k_scale = s->k_scale;
   a.v_scale = s->v_scale;
   a.out = out;

@@ -33,6 +33,7 @@
 // the V scale is folded into P (normalised by the step's largest scale, which
 // joins the running rescale), and the MMAs run in fp16.
 #include <cfloat>
+#include <climits>
 #include <mutex>
 
 #include "fa_internal.h"
@@ -48,6 +49,7 @@ struct DecCfg {
   static constexpr int TILE_BYTES = kTile * ROWB;       // one 16-row tile of K (or V)
   static constexpr int NT = 32768 / (2 * TILE_BYTES);   // tiles per pipeline step (32 KB of K+V)
   static constexpr int NSTAGE = 3;
+  static constexpr int PREFETCH_TILES = 2 * NSTAGE * NT; // tiles a CTA pulls into L2 before its dependency resolves
   static constexpr int NCW = 4;                         // consumer warps
   static constexpr int NTHR = (NCW + 1) * 32;
   static constexpr int QK_COLS = D * NT / NCW;          // QK^T columns per warp
@@ -72,6 +74,10 @@ struct DecK {
   const __nv_bfloat16* q;
   const int32_t* block_table;
   const int32_t* seq_lens;
+  const uint8_t* kb;    // slab bases and int8 scales, for L2 prefetch only
+  const uint8_t* vb;
+  const float* ksb;
+  const float* vsb;
   __nv_bfloat16* out;
   float* lse;
   int* counters;    // [U] arrival count per unit (null: no workspace, one CTA); zero between calls
@@ -140,6 +146,28 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sm, int* total) {
   __syncthreads();
   *total = tot;
   return base + incl - v;
+}
+
+// Block-wide (min, max) of one value per thread; sm holds 2 ints per warp.
+__device__ __forceinline__ int2 block_min_max(int mn, int mx, int* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    sm[2 * warp] = mn;
+    sm[2 * warp + 1] = mx;
+  }
+  __syncthreads();
+  int a = sm[0], b = sm[1];
+  for (int w = 1; w < nw; ++w) {
+    a = min(a, sm[2 * w]);
+    b = max(b, sm[2 * w + 1]);
+  }
+  __syncthreads();
+  return make_int2(a, b);
 }
 
 // Sequences of length <= 0 get out = 0 and lse = -inf; CTA `cta` of `ncta`
@@ -274,8 +302,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   uint64_t* empty = full + C::NSTAGE;
   uint64_t* qfull = empty + C::NSTAGE;
   uint64_t* qempty = qfull + 1;
-  __shared__ int sm_scan[8];
-  __shared__ int sh_u0, sh_p0, abort_flag, sh_last;
+  __shared__ int sm_scan[8], sm_mm[16];
+  __shared__ int sh_u0, sh_p0, sh_n0, abort_flag, sh_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -289,8 +317,14 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
 
   // ---------------------------------------------------------------- partition
   // One block scan gives every unit's first global tile P_u and the total T.
-  // When all units fit one pass (the usual case) the unit holding this CTA's
-  // first tile is found from it; otherwise a second pass finds it.
+  // Two ways to cut the tile lists into CTA shares:
+  //  * unit-aligned: when every unit has about the same number of tiles (the
+  //    sliding layers once L >= W), each unit is cut into kper equal parts,
+  //    one CTA each, so no CTA crosses a unit boundary and every merge has
+  //    exactly kper partials;
+  //  * concatenated: otherwise the lists are laid end to end and cut into
+  //    ncta equal shares, so every CTA moves the same bytes whatever the
+  //    length mix.
   int T = 0, my_n = 0, my_P = 0;
   {
     int running = 0;
@@ -311,7 +345,20 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
     }
     T = running;
   }
-  const int ncta = (T == 0) ? 0 : min(static_cast<int>(gridDim.x), max(1, (T + p.min_tiles - 1) / p.min_tiles));
+  int ncta = (T == 0) ? 0 : min(static_cast<int>(gridDim.x), max(1, (T + p.min_tiles - 1) / p.min_tiles));
+  int kper = 0;   // CTAs per unit of the unit-aligned cut (0: concatenated cut)
+  if (ncta > 0 && p.units <= static_cast<int>(blockDim.x)) {
+    const bool mine = static_cast<int>(threadIdx.x) < p.units;
+    const int2 r = block_min_max(mine ? my_n : INT_MAX, mine ? my_n : 0, sm_mm);
+    if (r.x >= 1 && r.y - r.x <= max(1, r.x >> 3)) {
+      const int k = min(ncta / p.units, r.x);
+      // take it only if it keeps at least 85% of the concatenated cut's CTAs
+      if (k >= 1 && 20 * k * p.units >= 17 * ncta) {
+        kper = k;
+        ncta = k * p.units;
+      }
+    }
+  }
   if (static_cast<int>(blockIdx.x) >= ncta) {
     if (ncta == 0 && blockIdx.x == 0) {   // nothing visible anywhere: only empty outputs to write
       griddep_wait();
@@ -319,9 +366,15 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
     }
     return;
   }
-  const long long s_beg = static_cast<long long>(blockIdx.x) * T / ncta;
-  const long long s_end = static_cast<long long>(blockIdx.x + 1) * T / ncta;
-  if (p.units <= static_cast<int>(blockDim.x)) {
+  long long s_beg = static_cast<long long>(blockIdx.x) * T / ncta;
+  long long s_end = static_cast<long long>(blockIdx.x + 1) * T / ncta;
+  if (kper) {
+    if (static_cast<int>(threadIdx.x) == static_cast<int>(blockIdx.x) / kper) {
+      sh_u0 = threadIdx.x;
+      sh_p0 = my_P;
+      sh_n0 = my_n;
+    }
+  } else if (p.units <= static_cast<int>(blockDim.x)) {
     if (my_n > 0 && my_P <= s_beg && s_beg < my_P + my_n) {
       sh_u0 = threadIdx.x;
       sh_p0 = my_P;
@@ -352,6 +405,11 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   }
   __syncthreads();
   const int u0 = sh_u0, p0 = sh_p0;
+  if (kper) {   // part r of unit u0
+    const int r = static_cast<int>(blockIdx.x) % kper, n0 = sh_n0;
+    s_beg = p0 + static_cast<long long>(r) * n0 / kper;
+    s_end = p0 + static_cast<long long>(r + 1) * n0 / kper;
+  }
 
   if (warp == C::NCW) {
     // ------------------------------------------------------------ producer
@@ -380,6 +438,20 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
             }
           }
           if (k0 == ta) {
+            if (j == 0 && p.early_metadata && k0 + lane < tz && lane < C::PREFETCH_TILES && pid >= 0) {
+              // While the preceding kernel finishes, pull this CTA's first
+              // tiles into L2.  A prefetch returns nothing to the SM, so it is
+              // safe even if that kernel is still writing the slab; the TMA
+              // loads below read only after the dependency resolves.
+              const size_t row0 = (static_cast<size_t>(pid) * p.Hkv + x.h) * p.page_size +
+                                  ((k0 + lane) % p.tiles_per_page) * kTile;
+              prefetch_l2(p.kb + row0 * C::ROWB, C::TILE_BYTES);
+              prefetch_l2(p.vb + row0 * C::ROWB, C::TILE_BYTES);
+              if constexpr (KV) {
+                prefetch_l2(p.ksb + row0, kTile * sizeof(float));
+                prefetch_l2(p.vsb + row0, kTile * sizeof(float));
+              }
+            }
             if (j == 0) griddep_wait();   // from here on q and the slab are read
             if (lane == 0) {
               if (j > 0) ok = mbar_wait(qempty, (j - 1) & 1);
@@ -684,7 +756,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
         if constexpr (!KV) return pv_d0 + mt * 16 + gid + 8 * half;
         else return pv_d0 + (mt >> 1) * 32 + 16 * half + 2 * gid + (mt & 1);
       };
-      const int c_first = cta_of(P, ncta, T), c_last = cta_of(P + x.n - 1, ncta, T);
+      const int c_first = kper ? u * kper : cta_of(P, ncta, T);
+      const int c_last = kper ? c_first + kper - 1 : cta_of(P + x.n - 1, ncta, T);
       if (c_first == c_last) {
         const float iA = (lA > 0.f) ? sigma / lA : 0.f, iB = (lB > 0.f) ? sigma / lB : 0.f;
 #pragma unroll
@@ -755,6 +828,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   k.q = static_cast<const __nv_bfloat16*>(a.q);
   k.block_table = a.block_table;
   k.seq_lens = a.seq_lens;
+  k.kb = static_cast<const uint8_t*>(a.k);
+  k.vb = static_cast<const uint8_t*>(a.v);
+  k.ksb = a.k_scale;
+  k.vsb = a.v_scale;
   k.out = static_cast<__nv_bfloat16*>(a.out);
   k.lse = a.lse;
   if (a.workspace) {

@@ -111,6 +111,8 @@ struct DecodeArgs {
   const void* q;
   const int32_t* block_table;
   const int32_t* seq_lens;
+  const void* k;   // slab bases (L2 prefetch before the launch dependency resolves)
+  const void* v;
   const float* k_scale;
   const float* v_scale;
   void* out;

@@ -106,6 +106,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned source) into L2.
+// No data reaches the SM and nothing is ordered with it, so it may be issued
+// before the data is known to be final.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding kernel's memory to be
 // visible; let the next kernel in the stream begin its launch.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
