@@ -124,6 +124,28 @@ static fa_status encode_slab_map(CUtensorMap* tm, void* base, int D, int kv_dtyp
   return FA_OK;
 }
 
+// The slab again, with the column block as the outermost dimension: dim0 =
+// one 128-byte column block, dim1 = row (stride D * elem), dim2 = column
+// block (stride 128 B).  A box (block, 16, D / block) is one 16-row tile that
+// lands as D / block consecutive 2 KB pieces of 16 rows x 128 B, each
+// 128-byte swizzled: the layout of the (block, 1, 16) boxes, in one copy.
+static fa_status encode_tile_map(CUtensorMap* tm, void* base, int D, int kv_dtype, uint64_t rows) {
+  auto enc = get_encoder();
+  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint64_t eb = elem_bytes(kv_dtype);
+  const uint64_t blk = 128 / eb;
+  cuuint64_t dims[3] = {blk, rows, static_cast<cuuint64_t>(D / blk)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * eb), 128};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(kTile), static_cast<cuuint32_t>(D / blk)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(tm, kv_dtype == FA_KV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (tile map) failed (CUresult %d)", (int)r);
+  return FA_OK;
+}
+
 // Queries q [N][Hq][D] as 4-D (64-column block elements, head, token, block
 // index): a box (64, g, 128/g, 1) lands as 128 rows ordered (token, head) x 128 B.
 static fa_status encode_q_map(CUtensorMap* tm, const void* q, int N, int Hq, int D, int g) {
@@ -336,6 +358,8 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
   if (st) return st;
   st = encode_slab_map(&s.tm_v, v, L.d.head_dim, c->kv_dtype, rows);
   if (st) return st;
+  if ((st = encode_tile_map(&s.tm_kt, k, L.d.head_dim, c->kv_dtype, rows))) return st;
+  if ((st = encode_tile_map(&s.tm_vt, v, L.d.head_dim, c->kv_dtype, rows))) return st;
   if (c->kv_dtype == FA_KV_INT8) {
     if ((st = encode_scale_map(&s.tm_ks, k_scale, rows))) return st;
     if ((st = encode_scale_map(&s.tm_vs, v_scale, rows))) return st;
@@ -427,8 +451,8 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.out = out;
   a.lse = lse;
   a.workspace = p.ws_bytes ? workspace : nullptr;
-  a.tm_k = &s->tm_k;
-  a.tm_v = &s->tm_v;
+  a.tm_k = &s->tm_kt;
+  a.tm_v = &s->tm_vt;
   a.tm_ks = &s->tm_ks;
   a.tm_vs = &s->tm_vs;
   a.B = B;

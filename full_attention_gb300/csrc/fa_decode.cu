@@ -64,7 +64,8 @@ struct DecCfg {
   static constexpr int OFF_Q = OFF_SC + NSTAGE * SC_BYTES;
   static constexpr int OFF_SX = OFF_Q + Q_BYTES;
   static constexpr int OFF_BAR = OFF_SX + SX_BYTES;
-  static constexpr int SMEM = OFF_BAR + (2 * NSTAGE + 2) * 8;
+  static constexpr int SMEM = OFF_BAR + (2 * NSTAGE + 3) * 8;
+  static constexpr int STAGE_ALL = NSTAGE * STAGE_KV;   // the ring, reused to stage a merge
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   static_assert(NT >= 1 && NCW % NT == 0 && 32 % NT == 0, "step shape");
   static_assert(QK_COLS % 32 == 0 && PV_COLS % 32 == 0, "warp column split");
@@ -190,12 +191,30 @@ __device__ void zero_empty_units(const DecK& p, int cta, int ncta, int tid, int 
 // consumer threads; wbuf is shared scratch of 8 * 128 + 16 floats.  Loads are
 // batched so that a typical merge (a handful of source CTAs) costs a few L2
 // round trips.
-template <int D>
-__device__ void merge_unit(const DecK& p, int u, const Unit& x, int nh, int head0, int cf, int cl, float* wbuf) {
+template <int D, int STAGE_BYTES>
+__device__ void merge_unit(const DecK& p, int u, const Unit& x, int nh, int head0, int cf, int cl, float* wbuf,
+                           uint8_t* stage, uint64_t* sbar, volatile int* abort_flag) {
   constexpr int CH = 128;                  // source CTAs per weight chunk
   constexpr int ITEMS = 8 * (D / 4) / 128; // float4 outputs per thread
+  constexpr int ROW_BYTES = 8 * D * 4;     // one source's o rows
+  constexpr int NB = STAGE_BYTES / ROW_BYTES;   // sources per staged batch
   const int tid = threadIdx.x;
   const int nct = cl - cf + 1;
+  // Staged path (the ring is idle and every weight fits one chunk): bulk
+  // copies bring NB sources' o rows into shared memory per batch, so a merge
+  // costs one L2 round trip per batch instead of one per source.
+  const bool staged = stage != nullptr && nct <= CH;
+  auto stage_batch = [&](int b0, int batch) {   // thread 0: request sources b0 .. b0 + n - 1
+    const int n = min(NB, nct - b0);
+    mbar_arrive_expect_tx(sbar, n * ROW_BYTES);
+    for (int c = 0; c < n; ++c)
+      bulk_load(stage + c * ROW_BYTES, p.o_part + (static_cast<size_t>(cf + b0 + c) + u) * 8 * D, ROW_BYTES, sbar);
+    (void)batch;
+  };
+  if (staged && tid == 0) {
+    fence_proxy_async_global();   // the other CTAs' rows, seen through the acquire, for the bulk copies
+    stage_batch(0, 0);
+  }
   const float2* mlg = reinterpret_cast<const float2*>(p.ml_part);
   float* Mh = wbuf + 8 * CH;
   float* Lh = Mh + 8;
@@ -241,7 +260,33 @@ __device__ void merge_unit(const DecK& p, int u, const Unit& x, int nh, int head
   float4 acc[ITEMS];
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < nct; c0 += CH) {
+  if (staged) {
+    for (int b0 = 0, batch = 0; b0 < nct; b0 += NB, ++batch) {
+      if (!mbar_wait(sbar, batch & 1)) *abort_flag = 1;
+      named_bar_sync(1, 128);
+      if (*abort_flag) {   // a copy that did not land in time: every thread leaves together
+        if (tid == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+        return;
+      }
+      const int n = min(NB, nct - b0);
+      for (int c = 0; c < n; ++c) {
+        const float* src = reinterpret_cast<const float*>(stage + c * ROW_BYTES);
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+          const int idx = tid + i * 128, hh = idx / (D / 4), d = (idx % (D / 4)) * 4;
+          const float w = wbuf[(b0 + c) * 8 + hh];
+          const float4 o = *reinterpret_cast<const float4*>(src + hh * D + d);
+          acc[i].x += w * o.x;
+          acc[i].y += w * o.y;
+          acc[i].z += w * o.z;
+          acc[i].w += w * o.w;
+        }
+      }
+      named_bar_sync(1, 128);   // every thread is done with this batch's rows
+      if (b0 + NB < nct && tid == 0) stage_batch(b0 + NB, batch + 1);
+    }
+  }
+  for (int c0 = 0; !staged && c0 < nct; c0 += CH) {
     const int n = min(CH, nct - c0);
     if (c0 > 0) {   // weights of later chunks (more than CH source CTAs)
       named_bar_sync(1, 128);
@@ -302,6 +347,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   uint64_t* empty = full + C::NSTAGE;
   uint64_t* qfull = empty + C::NSTAGE;
   uint64_t* qempty = qfull + 1;
+  uint64_t* mbar_merge = qempty + 1;
   __shared__ int sm_scan[8], sm_mm[16];
   __shared__ int sh_u0, sh_p0, sh_n0, abort_flag, sh_last;
 
@@ -400,6 +446,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
     }
     mbar_init(qfull, 1);
     mbar_init(qempty, C::NCW);
+    mbar_init(mbar_merge, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -478,11 +525,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
                 for (int t = 0; t < ntl; ++t) {
                   const int tile = k + t;
                   const int row0 = (pg[t] * p.Hkv + x.h) * p.page_size + (tile % p.tiles_per_page) * kTile;
-#pragma unroll
-                  for (int blk = 0; blk < C::NBLK; ++blk) {
-                    tma_load_3d(kdst + t * C::TILE_BYTES + blk * 2048, &tm_k, &full[st], 0, blk, row0, pol);
-                    tma_load_3d(vdst + t * C::TILE_BYTES + blk * 2048, &tm_v, &full[st], 0, blk, row0, pol);
-                  }
+                  // one copy per tile: all column blocks of 16 rows
+                  tma_load_3d(kdst + t * C::TILE_BYTES, &tm_k, &full[st], 0, row0, 0, pol);
+                  tma_load_3d(vdst + t * C::TILE_BYTES, &tm_v, &full[st], 0, row0, 0, pol);
                   if constexpr (KV) {
                     float* sc = reinterpret_cast<float*>(smem + C::OFF_SC + st * C::SC_BYTES);
                     tma_load_2d(sc + t * 32, &tm_ks, &full[st], 0, row0 / kTile, pol);
@@ -803,7 +848,12 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
           sh_last = last;
         }
         named_bar_sync(1, C::NCW * 32);
-        if (sh_last) merge_unit<D>(p, u, x, nh, head0, c_first, c_last, sx);
+        if (sh_last) {
+          // the ring is idle once this CTA's last segment is consumed: stage the merge there
+          const bool idle = P + x.n >= s_end;
+          merge_unit<D, C::STAGE_ALL>(p, u, x, nh, head0, c_first, c_last, sx, idle ? smem : nullptr, mbar_merge,
+                                       &abort_flag);
+        }
       }
     }
     ++j;

@@ -25,6 +25,11 @@ struct Slab {
   // row) with rows = num_pages * Hkv * page_size; see fa_cache_bind_slab.
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  // The same slabs as (column-block element, row, column block): one box is
+  // a whole 16-row tile, all column blocks, landing block-major like 16-row
+  // boxes of tm_k / tm_v side by side (one copy per tile).
+  CUtensorMap tm_kt;
+  CUtensorMap tm_vt;
   // int8 format: 2-D maps over the fp32 scales, one 16-float box per tile.
   CUtensorMap tm_ks;
   CUtensorMap tm_vs;

@@ -69,6 +69,12 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) accesses of the same bytes.
+// Order this thread's generic-proxy view of global memory (e.g. data made
+// visible by an acquire) before its later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
