@@ -1,9 +1,11 @@
 """Benchmark: paged decode attention (and chunked prefill) on GB300.
 
 One step = one decode step of the E2B-like workload through every layer:
-the KV store of the new token on the 7 owning layers, then paged decode
+the KV store of the new token on the 7 owning layers and paged decode
 attention on all 12 layers (7 owning + 5 KV-shared), batch 64, contexts
 U[512, 4096], 8 query heads / 1 KV head, sliding D 256 W 512 / full D 512.
+An owning layer's store runs inside its decode launch
+(fa_paged_decode_store_attn), so the step is 12 launches of decode_kernel.
 
 Prints one JSON line.  `value` is the achieved HBM bandwidth of the step:
 algorithmic bytes (KV the layers must read + q + out + the store's rows)
@@ -231,22 +233,19 @@ class DecodeStep:
             self.cache.store(i, k, v, part)
 
     def launches_per_step(self):
-        n = 0
-        for i, d in enumerate(self.layers):
-            if self.src[i] == i:
-                n += 1
-            n += 1
-        return n
+        return len(self.layers)   # one launch per layer: owning layers store their rows in it
 
     def run(self, events=None):
         for i in range(len(self.layers)):
-            if self.src[i] == i:
-                k, v, sl = self.new[i]
-                self.cache.store(i, k, v, sl)
             if events is not None:
                 events[i][0].record()
-            self.cache.decode(i, self.q[i], self.bt[i], self.lens_dev, self.max_len, self.out[i], self.lse[i],
-                              self.ws[i])
+            if self.src[i] == i:
+                k, v, sl = self.new[i]
+                self.cache.decode_store(i, self.q[i], k, v, sl, self.bt[i], self.lens_dev, self.max_len,
+                                        self.out[i], self.lse[i], self.ws[i])
+            else:
+                self.cache.decode(i, self.q[i], self.bt[i], self.lens_dev, self.max_len, self.out[i],
+                                  self.lse[i], self.ws[i])
             if events is not None:
                 events[i][1].record()
 
@@ -337,7 +336,11 @@ def gpu_arm(args, rank, world):
         t = sum(dec_ms[i] for i in idx) / 1e3 / n_ev
         per_kind[name] = {"launches_per_step": len(idx), "gb_per_s": round(b / t / 1e9, 1) if t else None,
                           "us_per_launch": round(t / len(idx) * 1e6, 2) if idx else None}
-    achieved = dec_bytes / dec_time / 1e9
+    # Every launch of the step is decode_kernel (stores run inside it), so
+    # its average launch duration in the step is the step time / launches;
+    # the event-bracketed graph above gives each layer's time run alone.
+    launch_bytes = step.step_bytes / nl
+    achieved = step.step_bytes / t_step / 1e9
     digest = source_digest("fa_decode.cu", "fa_ptx.cuh")
     traffic = profiled_traffic(f"decode_{args.workload}", digest)
     clocks = clk.summary()
@@ -359,8 +362,10 @@ def gpu_arm(args, rank, world):
         "roofline": {"kernel": "decode_kernel (paged decode attention, split-K merged in-kernel)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_source": peak_src,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": round(dec_bytes / nl),
-                     "per_kind": per_kind},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": round(launch_bytes),
+                     "avg_launch_us_in_step": round(t_step / nl * 1e6, 2),
+                     "per_kind_alone": per_kind,
+                     "alone_gb_per_s": round(dec_bytes / dec_time / 1e9, 1)},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),

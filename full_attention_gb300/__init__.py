@@ -55,6 +55,7 @@ def _load() -> ctypes.CDLL:
         "fa_kv_store": (i32, [vp, i32, vp, vp, vp, i32, vp]),
         "fa_decode_workspace_bytes": (sz, [vp, i32, i32, i32]),
         "fa_paged_decode_attn": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
+        "fa_paged_decode_store_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_attn_noalloc": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
         "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "fa_get_device_error": (i32, [ctypes.POINTER(i32), vp]),
@@ -177,6 +178,16 @@ class Cache:
         _check(_lib.fa_paged_decode_attn(self._h, layer, _p(q), _p(block_table), int(block_table.shape[1]),
                                          _p(seq_lens), int(q.shape[0]), int(max_seq_len), _p(out), _p(lse),
                                          _p(workspace), ws_bytes, _s(stream)))
+
+    def decode_store(self, layer: int, q, k_new, v_new, slot_mapping, block_table, seq_lens, max_seq_len: int,
+                     out, lse=None, workspace=None, stream=None) -> None:
+        """fa_paged_decode_store_attn: store the current token's k, v rows and
+        decode in one launch (owning layers; a shared layer only decodes)."""
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(_lib.fa_paged_decode_store_attn(self._h, layer, _p(q), _p(k_new), _p(v_new), _p(slot_mapping),
+                                               _p(block_table), int(block_table.shape[1]), _p(seq_lens),
+                                               int(q.shape[0]), int(max_seq_len), _p(out), _p(lse), _p(workspace),
+                                               ws_bytes, _s(stream)))
 
     def decode_noalloc(self, layer: int, q, block_table, seq_lens, max_seq_len: int, out, lse=None,
                        stream=None) -> None:

@@ -414,10 +414,13 @@ size_t fa_decode_workspace_bytes(const fa_cache* c, int32_t layer, int32_t B, in
   return plan_decode(c, layer, B, max_seq_len).ws_bytes;
 }
 
-fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const int32_t* block_table,
-                               int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t B,
-                               int32_t max_seq_len, void* out, float* lse, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+namespace fa {
+// Decode with an optional store of the current token (k_new, v_new, slots
+// non-null for an owning layer).
+static fa_status decode_call(fa_cache* c, int32_t layer, const void* q, const void* k_new, const void* v_new,
+                             const int32_t* slots, const int32_t* block_table, int32_t max_pages_per_seq,
+                             const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   fa_status st = check_layer(c, layer);
   if (st) return st;
   if (B < 0) return fail(FA_ERR_INVALID_ARG, "B must be >= 0");
@@ -446,6 +449,9 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.seq_lens = seq_lens;
   a.k = s->k;
   a.v = s->v;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slots = slots;
   a.k_scale = s->k_scale;
   a.v_scale = s->v_scale;
   a.out = out;
@@ -473,6 +479,34 @@ fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const 
   ce = launch_decode(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
   return ok();
+}
+}  // namespace fa
+
+fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const int32_t* block_table,
+                               int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t B,
+                               int32_t max_seq_len, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return decode_call(c, layer, q, nullptr, nullptr, nullptr, block_table, max_pages_per_seq, seq_lens, B,
+                     max_seq_len, out, lse, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_paged_decode_store_attn(fa_cache* c, int32_t layer, const void* q, const void* k_new,
+                                     const void* v_new, const int32_t* slot_mapping, const int32_t* block_table,
+                                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t B,
+                                     int32_t max_seq_len, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  fa_status st = check_layer(c, layer);
+  if (st) return st;
+  if (c->layers[layer].owner != layer)   // a shared layer: its source stored the rows earlier
+    return decode_call(c, layer, q, nullptr, nullptr, nullptr, block_table, max_pages_per_seq, seq_lens, B,
+                       max_seq_len, out, lse, workspace, workspace_bytes, stream);
+  if (B > 0) {
+    if (!k_new || !v_new || !slot_mapping)
+      return fail(FA_ERR_INVALID_ARG, "k_new, v_new, slot_mapping must be non-NULL for an owning layer");
+    if (!aligned16(k_new) || !aligned16(v_new)) return fail(FA_ERR_INVALID_ARG, "k_new, v_new must be 16-byte aligned");
+  }
+  return decode_call(c, layer, q, k_new, v_new, slot_mapping, block_table, max_pages_per_seq, seq_lens, B,
+                     max_seq_len, out, lse, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const void* k_ext, const void* v_ext,

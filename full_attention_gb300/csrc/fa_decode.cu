@@ -38,6 +38,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_row.cuh"
 
 namespace fa {
 
@@ -75,10 +76,13 @@ struct DecK {
   const __nv_bfloat16* q;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  const uint8_t* kb;    // slab bases and int8 scales, for L2 prefetch only
-  const uint8_t* vb;
-  const float* ksb;
-  const float* vsb;
+  uint8_t* kb;    // slab bases and int8 scales (L2 prefetch, the current token's store)
+  uint8_t* vb;
+  float* ksb;
+  float* vsb;
+  const __nv_bfloat16* k_new;   // current token's rows [B][Hkv][D] and their slots, stored by
+  const __nv_bfloat16* v_new;   // the CTA that reads the unit's last tile (null: no store)
+  const int32_t* slots;
   __nv_bfloat16* out;
   float* lse;
   int* counters;    // [U] arrival count per unit (null: no workspace, one CTA); zero between calls
@@ -173,11 +177,39 @@ __device__ __forceinline__ int2 block_min_max(int mn, int mx, int* sm) {
 
 // Sequences of length <= 0 get out = 0 and lse = -inf; CTA `cta` of `ncta`
 // writes the units u with u % ncta == cta.
-template <int D>
+// The current token's K and V rows of (sequence b, KV head h) into slot `slot`
+// (one warp; slot < 0 skips, a slot past the pool is reported).
+template <int D, int KV>
+__device__ __forceinline__ void store_current(const DecK& p, const RowRegs<D>& rk, const RowRegs<D>& rv, int h,
+                                              int slot, int lane) {
+  if (slot < 0) return;
+  const int page = slot / p.page_size, off = slot % p.page_size;
+  if (page >= p.num_pages) {
+    if (lane == 0) atomicOr(p.err, FA_DEV_ERR_SLOT);
+    return;
+  }
+  const size_t row = (static_cast<size_t>(page) * p.Hkv + h) * p.page_size + off;
+  if constexpr (KV) {
+    row_store_int8<D>(rk, reinterpret_cast<int8_t*>(p.kb) + row * D, p.ksb + row, lane);
+    row_store_int8<D>(rv, reinterpret_cast<int8_t*>(p.vb) + row * D, p.vsb + row, lane);
+  } else {
+    row_store_bf16<D>(rk, reinterpret_cast<__nv_bfloat16*>(p.kb) + row * D, lane);
+    row_store_bf16<D>(rv, reinterpret_cast<__nv_bfloat16*>(p.vb) + row * D, lane);
+  }
+}
+
+template <int D, int KV>
 __device__ void zero_empty_units(const DecK& p, int cta, int ncta, int tid, int nthr) {
   for (int u = cta; u < p.units; u += ncta) {
     const Unit x = unit_of(p, u);
     if (x.L > 0) continue;
+    if (p.slots && x.c == 0 && tid < 32) {   // nothing to attend, but the row is still stored
+      RowRegs<D> rk, rv;
+      const size_t src = (static_cast<size_t>(x.b) * p.Hkv + x.h) * D;
+      row_load<D>(rk, p.k_new + src, tid);
+      row_load<D>(rv, p.v_new + src, tid);
+      store_current<D, KV>(p, rk, rv, x.h, __ldg(p.slots + x.b), tid);
+    }
     const int nh = min(8, p.g - x.c * 8), head0 = x.h * p.g + x.c * 8;
     for (int i = tid; i < nh * D; i += nthr)
       p.out[(static_cast<size_t>(x.b) * p.Hq + head0 + i / D) * D + i % D] = __float2bfloat16(0.0f);
@@ -408,7 +440,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   if (static_cast<int>(blockIdx.x) >= ncta) {
     if (ncta == 0 && blockIdx.x == 0) {   // nothing visible anywhere: only empty outputs to write
       griddep_wait();
-      zero_empty_units<D>(p, 0, 1, threadIdx.x, blockDim.x);
+      zero_empty_units<D, KV>(p, 0, 1, threadIdx.x, blockDim.x);
     }
     return;
   }
@@ -475,6 +507,12 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
         const int tz = x.t_first + static_cast<int>(min(s_end, P + x.n) - P);
         const int nh = min(8, p.g - x.c * 8), head0 = x.h * p.g + x.c * 8;
         const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
+        // The CTA that reads the unit's last tile (it holds position L - 1)
+        // stores the current token's rows first, so its own copy of that
+        // tile sees them.
+        const bool store_here = p.slots != nullptr && tz == x.t_first + x.n;
+        bool stored = false;
+        RowRegs<D> rk, rv;
         for (int k0 = ta; ok && k0 < tz; k0 += 32) {
           int pid = -1;
           if (k0 + lane < tz) {
@@ -509,9 +547,22 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
+            if (store_here) {   // issue the row loads now; they are written before the last tile's copy
+              const size_t src = (static_cast<size_t>(x.b) * p.Hkv + x.h) * D;
+              row_load<D>(rk, p.k_new + src, lane);
+              row_load<D>(rv, p.v_new + src, lane);
+            }
           }
           for (int k = k0; k < min(k0 + 32, tz); k += C::NT) {
             const int ntl = min(C::NT, tz - k);
+            if (store_here && !stored && k + ntl >= tz) {
+              stored = true;
+              store_current<D, KV>(p, rk, rv, x.h, __ldg(p.slots + x.b), lane);
+              // each lane orders its generic writes before the async-proxy
+              // (TMA) read of the tile that holds them
+              fence_proxy_async_global();
+              __syncwarp();
+            }
             int pg[C::NT];
 #pragma unroll
             for (int t = 0; t < C::NT; ++t) pg[t] = __shfl_sync(0xffffffffu, pid, (k - k0 + t) & 31);
@@ -557,7 +608,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
 
   // -------------------------------------------------------------- consumers
   griddep_wait();
-  zero_empty_units<D>(p, blockIdx.x, ncta, threadIdx.x, C::NCW * 32);
+  zero_empty_units<D, KV>(p, blockIdx.x, ncta, threadIdx.x, C::NCW * 32);
   const int qk_tile = warp % C::NT;
   const int qk_d0 = (warp / C::NT) * C::QK_COLS;
   const int pv_d0 = warp * C::PV_COLS;
@@ -620,7 +671,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
       }
 
       // ---- partial S^T over this warp's columns
+      // two accumulator chains (even / odd column steps) halve the dependent MMA chain
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc1[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok && qk_tile < ntl) {
         const uint8_t* kt = ks + qk_tile * C::TILE_BYTES;
         const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -630,7 +683,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
           if constexpr (!KV) {
             const int dc = qk_d0 + kk * 16 + (lane >> 4) * 8;
             ldsm_x4(smem_u32(kt + (dc >> 6) * 2048 + sw128(r, (dc & 63) >> 3)), a0, a1, a2, a3);
-            mma_bf16(acc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            mma_bf16((kk & 1) ? acc1 : acc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
           } else {
             const int dc = qk_d0 + kk * 32 + (lane >> 4) * 16;
             ldsm_x4(smem_u32(kt + (dc >> 7) * 2048 + sw128(r, (dc & 127) >> 4)), a0, a1, a2, a3);
@@ -638,11 +691,13 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
             const uint32_t x2 = a2 ^ 0x80808080u, x3 = a3 ^ 0x80808080u;
             mma_f16(acc, i8pair_to_f16x2(x0, 0x4140), i8pair_to_f16x2(x1, 0x4140), i8pair_to_f16x2(x0, 0x4342),
                     i8pair_to_f16x2(x1, 0x4342), qf[kk][0], qf[kk][1]);
-            mma_f16(acc, i8pair_to_f16x2(x2, 0x4140), i8pair_to_f16x2(x3, 0x4140), i8pair_to_f16x2(x2, 0x4342),
+            mma_f16(acc1, i8pair_to_f16x2(x2, 0x4140), i8pair_to_f16x2(x3, 0x4140), i8pair_to_f16x2(x2, 0x4342),
                     i8pair_to_f16x2(x3, 0x4342), qf[kk][2], qf[kk][3]);
           }
         }
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += acc1[i];
       float* sxw = sx + (buf * C::NCW + warp) * kTile * C::SX_STRIDE;
       *reinterpret_cast<float2*>(sxw + gid * C::SX_STRIDE + 2 * tig) = make_float2(acc[0], acc[1]);
       *reinterpret_cast<float2*>(sxw + (gid + 8) * C::SX_STRIDE + 2 * tig) = make_float2(acc[2], acc[3]);
@@ -878,10 +933,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   k.q = static_cast<const __nv_bfloat16*>(a.q);
   k.block_table = a.block_table;
   k.seq_lens = a.seq_lens;
-  k.kb = static_cast<const uint8_t*>(a.k);
-  k.vb = static_cast<const uint8_t*>(a.v);
-  k.ksb = a.k_scale;
-  k.vsb = a.v_scale;
+  k.kb = static_cast<uint8_t*>(const_cast<void*>(a.k));
+  k.vb = static_cast<uint8_t*>(const_cast<void*>(a.v));
+  k.ksb = const_cast<float*>(a.k_scale);
+  k.vsb = const_cast<float*>(a.v_scale);
+  k.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  k.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  k.slots = a.slots;
   k.out = static_cast<__nv_bfloat16*>(a.out);
   k.lse = a.lse;
   if (a.workspace) {

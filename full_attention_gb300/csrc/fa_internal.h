@@ -116,8 +116,11 @@ struct DecodeArgs {
   const void* q;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  const void* k;   // slab bases (L2 prefetch before the launch dependency resolves)
+  const void* k;   // slab bases (L2 prefetch, the current token's store)
   const void* v;
+  const void* k_new;        // fused store of the current token (null: none)
+  const void* v_new;
+  const int32_t* slots;
   const float* k_scale;
   const float* v_scale;
   void* out;

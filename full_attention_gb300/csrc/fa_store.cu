@@ -11,6 +11,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_row.cuh"
 
 // Device error word: FA_DEV_ERR_* bits OR-ed in by every kernel of the library.
 __device__ unsigned int g_fa_device_error;
@@ -59,26 +60,14 @@ __global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
     return;
   }
   griddep_wait();   // the rows (and the slab) may belong to the previous kernel
-  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(which ? a.v : a.k) +
-                                                    (static_cast<size_t>(t) * a.Hkv + h) * D);
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) +
-                                        ((static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off) * D);
-#pragma unroll
-  for (int i = 0; i < D / 256; ++i) dst[i * 32 + lane] = __ldg(src + i * 32 + lane);
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&x)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+  RowRegs<D> r;
+  row_load<D>(r, static_cast<const __nv_bfloat16*>(which ? a.v : a.k) + (static_cast<size_t>(t) * a.Hkv + h) * D, lane);
+  row_store_bf16<D>(r, static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) +
+                           ((static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off) * D, lane);
 }
 
 template <int D>
 __global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
-  constexpr int NV = D / 256;            // 16-byte vectors (8 values) per lane
   if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -96,37 +85,11 @@ __global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
     return;
   }
   griddep_wait();   // the rows (and the slab) may belong to the previous kernel
-  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(which ? a.v : a.k) +
-                                                    (static_cast<size_t>(t) * a.Hkv + h) * D);
-  float x[NV][8];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    bf16x8_to_f32(__ldg(src + i * 32 + lane), x[i]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s = __fdiv_rn(amax, 127.0f);
+  RowRegs<D> r;
+  row_load<D>(r, static_cast<const __nv_bfloat16*>(which ? a.v : a.k) + (static_cast<size_t>(t) * a.Hkv + h) * D, lane);
   const size_t row = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
-  int8_t* dst = static_cast<int8_t*>(which ? a.v_slab : a.k_slab) + row * D;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      int c = 0;
-      if (amax != 0.0f) {
-        float qv = rintf(__fdiv_rn(x[i][e], s));
-        qv = fminf(fmaxf(qv, -127.0f), 127.0f);
-        c = static_cast<int>(qv);
-      }
-      packed[e >> 2] |= (static_cast<uint32_t>(c) & 0xffu) << (8 * (e & 3));
-    }
-    *reinterpret_cast<uint2*>(dst + i * 256 + lane * 8) = make_uint2(packed[0], packed[1]);
-  }
-  if (lane == 0) (which ? a.v_scale : a.k_scale)[row] = s;
+  row_store_int8<D>(r, static_cast<int8_t*>(which ? a.v_slab : a.k_slab) + row * D,
+                    (which ? a.v_scale : a.k_scale) + row, lane);
 }
 
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {

@@ -220,6 +220,29 @@ FA_API fa_status fa_paged_decode_attn(fa_cache* cache, int32_t layer, const void
                                void* out, float* lse, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Store and decode in one launch: the effect of fa_kv_store(cache, layer,
+ * k_new, v_new, slot_mapping, B) followed by fa_paged_decode_attn with the
+ * same remaining arguments, for an owning layer, without a second kernel on
+ * the dependency chain of the step ("FreeToken PR #898", description: each
+ * owning layer stores its rows, then attends; the pages order store before
+ * attend).  k_new, v_new: bf16 [B][Hkv][D], the current token's post-RoPE
+ * rows (device, 16-byte aligned); slot_mapping: int32 [B], the slot of
+ * position seq_lens[b] - 1 (negative: not stored; past the pool: not stored,
+ * FA_DEV_ERR_SLOT).  The slot must be the one the block table gives for that
+ * position, as with the two separate calls.  Rows are stored in the slab's
+ * format (bf16 copy, or the int8 quantisation of fa_kv_store, bit for bit)
+ * by the CTA that reads the tile holding that position, before it reads it;
+ * sequences with seq_lens[b] <= 0 still get their row stored.  For a shared
+ * layer k_new, v_new and slot_mapping are ignored (may be NULL) and the call
+ * is fa_paged_decode_attn.  Workspace, outputs and errors as
+ * fa_paged_decode_attn. */
+FA_API fa_status fa_paged_decode_store_attn(fa_cache* cache, int32_t layer, const void* q,
+                                     const void* k_new, const void* v_new,
+                                     const int32_t* slot_mapping, const int32_t* block_table,
+                                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t B,
+                                     int32_t max_seq_len, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* Largest scratch the allocation-free decode below can use (bytes). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

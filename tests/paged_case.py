@@ -149,6 +149,23 @@ class DecodeCase:
         self.cache.decode(i, self.q[i], self.bt_dev[i], self.lens_dev, self.max_len, out, lse, ws)
         return out, lse
 
+    def decode_store(self, i, out=None, lse=None, ws=None, slots=None):
+        """The fused call: store layer i's current rows (owning layer) and decode."""
+        d = self.layers[i]
+        if out is None:
+            out = torch.empty((self.B, d["num_q_heads"], d["head_dim"]), dtype=torch.bfloat16, device=self.device)
+        if lse is None:
+            lse = torch.empty((self.B, d["num_q_heads"]), dtype=torch.float32, device=self.device)
+        if ws is None:
+            ws = self.workspace(i)
+        if self.src[i] == i:
+            k, v = self.new_kv[i]
+            sl = self.slot_mapping(i) if slots is None else slots
+        else:
+            k = v = sl = None
+        self.cache.decode_store(i, self.q[i], k, v, sl, self.bt_dev[i], self.lens_dev, self.max_len, out, lse, ws)
+        return out, lse
+
     # -- oracle -------------------------------------------------------------
     def oracle_decode(self, i, seqs):
         """Oracle outputs of layer i for the sequences `seqs` (all heads),
