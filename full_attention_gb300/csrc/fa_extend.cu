@@ -12,14 +12,20 @@
 // times the g query heads that share the KV head (GQA packed into the M
 // dimension, so each K/V tile serves all g heads), and one 256-column slice of
 // the output (head_dim 512 uses two CTAs, each recomputing S over the full
-// head_dim; a 128 x 512 fp32 O would fill all of tensor memory).  Roles:
-//   warp 0      TMA producer: Q once (4-D map, rows = (token, head)); per
-//               64-key tile the K tile in 64-column chunks and the V tile of
-//               this CTA's output slice, from slab pages or from k_ext / v_ext;
+// head_dim; a 128 x 512 fp32 O would fill all of tensor memory).
+// Tensor memory (512 columns): O [0, 256), two S/P buffers [256, 384), and
+// the first 256 columns of Q as bf16 pairs [384, 512), so S = Q K^T reads
+// that part of Q from tensor memory and only the rest (head_dim 512) from
+// shared memory; the freed shared memory deepens the K/V ring.  Roles:
+//   warp 0      TMA producer: the shared-memory part of Q once (4-D map,
+//               rows = (token, head)); per 64-key tile the K tile in
+//               64-column chunks and the V tile of this CTA's output slice,
+//               from slab pages or from k_ext / v_ext;
 //   warp 1      MMA issuer: S_j = Q K_j^T (tcgen05.mma, M=128, N=64, fp32 in
 //               TMEM, double buffered), then O += P_{j-1} V_{j-1} with P read
 //               from tensor memory and V as an MN-major operand (N=256);
-//   warps 2-5   softmax: one query row per thread; load S from TMEM, mask,
+//   warps 2-5   softmax: one query row per thread; first copy the row's
+//               leading 256 Q values into tensor memory; per tile load S, mask,
 //               online softmax in the log2 domain, write P (bf16) back into the
 //               S buffer; rescale O in TMEM only when the running max grows by
 //               more than 2^8, so rescales are rare; final normalisation and
@@ -38,25 +44,37 @@ struct ExtCfg {
   static constexpr int NK = 64;                 // keys per tile
   static constexpr int DS = 256;                // output columns per CTA
   static constexpr int KB = D / 64;             // 64-column blocks of head_dim
-  static constexpr int Q_BYTES = M * D * 2;     // [KB][128][64] bf16
+  static constexpr int NQT = 4;                 // Q blocks held in tensor memory
+  static constexpr int NQS = KB - NQT;          // Q blocks held in shared memory
+  static constexpr int Q_BYTES = NQS * M * 128; // [NQS][128][64] bf16
   static constexpr int SLOT = NK * 64 * 2;      // one ring slot: 64 keys x 64 columns (a K chunk or a V block)
-  static constexpr int BAR_BYTES = 512;
+  static constexpr int BAR_BYTES = 1024;
   // the rest of shared memory is a ring of slots; per tile KB K chunks and 4 V blocks pass through it
   static constexpr int NSLOT = (232448 - 1024 - Q_BYTES - BAR_BYTES) / SLOT;
   static constexpr int OFF_RING = Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
-  static constexpr int NTHR = 6 * 32;
-  // tensor memory columns: O [0, 256), S/P buffers [256, 320) and [320, 384)
+  static constexpr int NPW = 4;                 // producer warps
+  static constexpr int W_MMA = NPW;             // the MMA warp; the softmax warps follow it
+  static constexpr int NTHR = (NPW + 1 + 4) * 32;
+  // tensor memory columns: O [0, 256), S/P buffers [256, 320) and [320, 384),
+  // Q blocks 0..NQT-1 [384, 512) (32 columns of bf16 pairs each)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t S_COL0 = 256;
+  static constexpr uint32_t Q_COL0 = 384;
+  static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static_assert((1 + 2 * NSLOT + 2 + 2 + 2) * 8 <= BAR_BYTES, "barrier space");
+  static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1) * 8 <= BAR_BYTES, "barrier space");
   static_assert(NSLOT >= KB + 4, "a ring must hold one tile");
 };
 
 struct ExtK {
+  const __nv_bfloat16* q;
+  const uint8_t* k_slab;   // [rows][D] bf16, rows = (page * Hkv + head) * page_size + offset
+  const uint8_t* v_slab;
+  const uint8_t* k_ext;    // [num_tokens][Hkv][D] bf16
+  const uint8_t* v_ext;
   const int32_t* qo_indptr;
   const int32_t* prefix_lens;
   const int32_t* block_table;
@@ -64,20 +82,32 @@ struct ExtK {
   float* lse;
   unsigned int* err;
   int B, Hq, Hkv, g, T, kind, window, page_size, tiles_per_page, num_pages, max_pages_per_seq;
-  int max_q_len, max_prefix_len, dslices, early_metadata;
+  int max_q_len, max_prefix_len, dslices, early_metadata, num_tokens;
   float scale_log2;
 };
 
 // The key tiles one CTA walks: prefix tiles (16-aligned starts, from the
 // slab) then chunk tiles (64-aligned relative to P, from k_ext / v_ext).
+// The CTAs of one (sequence, KV head) read the same prefix tiles; each walks
+// them from a different starting tile (rot), so at any moment they read
+// different lines and the L2 slices share the load.  The softmax does not
+// depend on the order of the tiles.
 struct ExtPlan {
   int b, h, ds, t0, n, P, qo0;
   int kmin, kmax;          // visible key positions of the CTA's rows
   int a0, np;              // first prefix tile start, number of prefix tiles
   int c0, nc;              // first chunk tile start (absolute position), number of chunk tiles
+  int rot;                 // walk prefix tiles from tile rot, wrapping
   __device__ int tiles() const { return np + nc; }
   __device__ bool prefix(int j) const { return j < np; }
-  __device__ int start(int j) const { return j < np ? a0 + 64 * j : c0 + 64 * (j - np); }
+  __device__ int start(int j) const {
+    if (j < np) {
+      int k = j + rot;
+      if (k >= np) k -= np;
+      return a0 + 64 * k;
+    }
+    return c0 + 64 * (j - np);
+  }
 };
 
 __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
@@ -104,6 +134,7 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   const int cfirst = max(x.kmin, x.P);
   x.c0 = x.P + ((cfirst - x.P) / 64) * 64;
   x.nc = (x.kmax >= x.c0) ? (x.kmax - x.c0) / 64 + 1 : 0;
+  x.rot = x.np > 1 ? static_cast<int>((blockIdx.x * 2u + x.ds) * 5u % static_cast<unsigned>(x.np)) : 0;
   return true;
 }
 
@@ -123,8 +154,9 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   uint64_t* s_full = empty + C::NSLOT;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_bar = p_full + 2;
+  uint64_t* qt_full = o_bar + 2;        // the softmax warps have put Q into tensor memory
   __shared__ uint32_t tmem_slot;
-  __shared__ uint64_t done_bar, san_bar;
+  __shared__ uint64_t done_bar;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!p.early_metadata) griddep_wait();
@@ -136,7 +168,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], 33);   // the filling warp: lane 0's expect_tx + 32 lane arrivals
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -145,122 +177,165 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     }
     mbar_init(&o_bar[0], 1);
     mbar_init(&o_bar[1], 1);
+    mbar_init(qt_full, 4);
     mbar_init(&done_bar, 1);
-    mbar_init(&san_bar, 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  if (warp == C::W_MMA) tmem_alloc(&tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   griddep_wait();   // from here on q, k, v, the slab and the outputs are touched
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp < C::NPW) {
+    // ----------------------------------------------------------- producers
     // Emission order = the MMA issuer's consumption order: K_0, then for each
-    // t >= 1: K_t (if any) and V_{t-1}.  Page ids are loaded a tile ahead.
-    const uint64_t pol = l2_policy_evict_last();   // K/V tiles are shared by the CTAs of a (sequence, head)
-    int e = 0;
-    bool ok = true;
-    if (lane == 0) {
+    // t >= 1: K_t (if any) and V_{t-1}.  A slot is one 64-key x 64-column
+    // block in the 128-byte-swizzled K-major layout, filled by one producer
+    // warp (slot e by warp e % NPW): TMA boxes of 16 rows from the slab (one
+    // per page), or one box of 64 rows from k_ext / v_ext.  A single thread
+    // issues TMA copies at a rate that caps the fill far below what the MMAs
+    // consume; four issuing warps do not.  The page that holds the prefix end
+    // also holds slots past it (stale values, possibly NaN, that the PV MMA
+    // would multiply by zero): its 16 rows are copied by the warp's lanes
+    // with cp.async, zero-filling rows at or past the prefix end.
+    // full[] counts 33 arrivals: lane 0's expect_tx, then 32 lane arrivals
+    // (when their cp.async copies land, or at once when there are none).
+    const int pw = warp;
+    const uint64_t pol = l2_policy_evict_last();   // K/V rows are shared by the CTAs of a (sequence, head)
+    if (threadIdx.x == 0) {
       prefetch_tmap(&tm_q);
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_4d(qs + kb * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
+      for (int kb = C::NQT; kb < C::KB; ++kb)
+        tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
+    }
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_kx);
+      prefetch_tmap(&tm_vx);
     }
     const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
-    auto load_pid = [&](int j) -> int {   // lanes 0-3: page of 16-row box `lane` of tile j
+    // page ids of tile j's 4 row groups, lanes 0-3 (-1: not a prefix row; -2: bad page id)
+    auto load_pid = [&](int j) -> int {
       int pid = -1;
       if (j < nt && x.prefix(j) && lane < 4) {
-        const int pos = x.start(j) + 16 * lane;
-        if (pos < x.P) {
-          pid = __ldg(bt + pos / p.page_size);
-          if (pid < 0 || pid >= p.num_pages) {
-            atomicOr(p.err, FA_DEV_ERR_PAGE);
-            pid = -1;   // outside the tensor: the box reads zeros
-          }
-        }
+        const int pos = x.start(j) + 16 * lane;   // a 16-row group lies in one page
+        if (pos < x.P) pid = __ldg(bt + pos / p.page_size);   // checked where it is used, a tile later
       }
       return pid;
     };
-    auto rows_of = [&](int j, int pid, int (&row0)[4]) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int pg = __shfl_sync(0xffffffffu, pid, i);
-        row0[i] = (pg * p.Hkv + x.h) * p.page_size + ((x.start(j) + 16 * i) % p.page_size);
-      }
+    struct TileSrc {
+      int row0[4];   // slab row of each 16-row group (prefix tiles), -1: no page
+      int lim;       // rows [0, lim) of the tile hold keys (prefix: < P)
+      int bgroup;    // the group holding the prefix end inside it, -1: none
+      bool prefix;
+      int tok0;      // chunk tiles: first token row in k_ext / v_ext
     };
-    // one ring slot: wait for it to be free, then fill it with a K chunk or V block
-    auto emit = [&](int j, int blk, bool is_v, const int (&row0)[4]) {
-      const int sl = e % C::NSLOT;
-      ok = ok && mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
-      if (!ok) return;
-      mbar_arrive_expect_tx(&full[sl], C::SLOT);
-      uint8_t* dst = ring + sl * C::SLOT;
-      const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-      if (x.prefix(j)) {
+    auto tile_src = [&](int j, int pid) {
+      TileSrc ts;
+      const int st0 = x.start(j);
+      ts.prefix = x.prefix(j);
+      ts.lim = ts.prefix ? x.P - st0 : x.n - (st0 - x.P);
+      ts.bgroup = (ts.prefix && ts.lim < 64 && (ts.lim & 15) != 0) ? (ts.lim >> 4) : -1;
+      ts.tok0 = x.qo0 + st0 - x.P;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tma_load_3d(dst + i * 2048, tm, &full[sl], 0, blk, row0[i], pol);
-      } else {
-        tma_load_4d(dst, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, x.qo0 + (x.start(j) - x.P), pol);
+      for (int g = 0; g < 4; ++g) {
+        int pg = __shfl_sync(0xffffffffu, pid, g);
+        if (ts.prefix && 16 * g < ts.lim && (pg < 0 || pg >= p.num_pages)) {   // a bad page id reads as zeros
+          if (pw == 0 && lane == 0) atomicOr(p.err, FA_DEV_ERR_PAGE);
+          pg = -1;
+        }
+        ts.row0[g] = pg >= 0 ? (pg * p.Hkv + x.h) * p.page_size + (st0 + 16 * g) % p.page_size : -1;
+      }
+      return ts;
+    };
+    int e = 0;
+    bool ok = true;
+    auto emit = [&](const TileSrc& ts, int blk, bool is_v) {
+      if (e % C::NPW == pw) {
+        const int sl = e % C::NSLOT;
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+        ok = __shfl_sync(0xffffffffu, w, 0) && ok;
+        if (ok) {
+          uint8_t* dst = ring + sl * C::SLOT;
+          if (ts.prefix) {
+            if (lane == 0) {
+              int tx = 0;
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim) tx += 2048;
+              mbar_arrive_expect_tx(&full[sl], tx);
+#pragma unroll
+              for (int g = 0; g < 4; ++g)
+                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim)
+                  tma_load_3d(dst + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk, ts.row0[g], pol);
+            }
+            // groups without a page (or past the prefix) must read as zero: the slot holds older data
+            const uint8_t* base = is_v ? p.v_slab : p.k_slab;
+            bool any_cp = false;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const bool tma = g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim;
+              if (tma) continue;
+              any_cp = true;
+              // 16 rows x 8 units: lane copies rows lane / 8 + 4 i, unit lane % 8
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
+                const bool v = ts.row0[g] >= 0 && r < ts.lim;
+                const uint8_t* src = base + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + blk * 64) * 2 + (lane & 7) * 16 : 0);
+                cp_async16_zfill(dst + sw128(r, lane & 7), src, v, pol);
+              }
+            }
+            if (any_cp) cp_async_mbar_arrive(&full[sl]);
+            else if (lane == 0) mbar_arrive_n(&full[sl], 32);
+          } else {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&full[sl], C::SLOT);
+              tma_load_4d(dst, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, ts.tok0, pol);
+              mbar_arrive_n(&full[sl], 32);
+            }
+          }
+        }
       }
       ++e;
     };
     int pid_next = load_pid(0);
-    int row_cur[4], row_prev[4];
+    TileSrc src_cur{}, src_prev{};
     for (int t = 0; ok && t <= nt; ++t) {
       if (t < nt) {
         const int pid = pid_next;
-        pid_next = load_pid(t + 1);
-        rows_of(t, pid, row_cur);
-        if (lane == 0)
-          for (int kb = 0; ok && kb < C::KB; ++kb) emit(t, kb, false, row_cur);
+        pid_next = load_pid(t + 1);   // a tile ahead
+        src_cur = tile_src(t, pid);
+        for (int kb = 0; ok && kb < C::KB; ++kb) emit(src_cur, kb, false);
       }
-      if (t >= 1 && lane == 0)
-        for (int i4 = 0; ok && i4 < 4; ++i4) emit(t - 1, x.ds * 4 + i4, true, row_prev);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      const int jb = t - 1;
-      if (ok && t >= 1 && x.prefix(jb) && x.start(jb) + 64 > x.P && (x.P & 15) != 0) {
-        // The last prefix page's slots at positions >= P hold whatever they held
-        // before (their P is 0, but NaN * 0 is NaN in the MMA): wait for this
-        // tile's V blocks to land and zero those rows, then release the softmax.
-        const int e_last = __shfl_sync(0xffffffffu, e, 0);
-        const int r0 = x.P - x.start(jb), r1 = min(64, ((x.P + 15) & ~15) - x.start(jb));
-        for (int i4 = 0; i4 < 4; ++i4) {
-          const int idx = e_last - 4 + i4, sl = idx % C::NSLOT;
-          bool landed = true;
-          if (lane == 0) landed = mbar_wait(&full[sl], (idx / C::NSLOT) & 1);
-          ok = __shfl_sync(0xffffffffu, landed, 0) && ok;
-          if (!ok) break;
-          uint8_t* vt = ring + sl * C::SLOT;
-          for (int u = lane; u < (r1 - r0) * 8; u += 32)
-            *reinterpret_cast<uint4*>(vt + sw128(r0 + u / 8, u % 8)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(&san_bar);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) row_prev[i] = row_cur[i];
+      if (t >= 1)
+        for (int i4 = 0; ok && i4 < 4; ++i4) emit(src_prev, x.ds * 4 + i4, true);
+      src_prev = src_cur;
     }
+    if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    // drain: no copy may still be landing when the CTA exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (lane == 0) {
-      if (!ok) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-      // drain: no bulk copy may still be landing when the CTA exits
-      if (!mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
       for (int i = max(0, e - C::NSLOT); i < e; ++i)
-        if (!mbar_wait(&full[i % C::NSLOT], (i / C::NSLOT) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+        if (i % C::NPW == pw && !mbar_wait(&full[i % C::NSLOT], (i / C::NSLOT) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     }
-  } else if (warp == 1) {
+    if (threadIdx.x == 0 && !mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+  } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);
       const uint32_t idO = umma_idesc_bf16(C::M, 64, true);
-      bool ok = mbar_wait(q_full, 0);
+      bool ok = mbar_wait(q_full, 0) && mbar_wait(qt_full, 0);
+      tc_fence_after();
       int e = 0;
       auto take = [&]() -> uint32_t {   // wait for the next ring slot, return its address
         const int sl = e % C::NSLOT;
         ok = ok && mbar_wait(&full[sl], (e / C::NSLOT) & 1);
+        fence_proxy_async_smem();   // the cp.async writes, seen through the barrier, for the MMA's reads
         tc_fence_after();
         return smem_u32(ring + sl * C::SLOT);
       };
@@ -277,11 +352,18 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
           for (int kb = 0; ok && kb < C::KB; ++kb) {
             const uint32_t kbase = take();
             if (!ok) break;
-            const uint32_t qb = smem_u32(qs + kb * (C::M * 128));
+            if (kb < C::NQT) {   // A = Q block from tensor memory
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024),
-                      idS, (kb > 0 || ks > 0) ? 1u : 0u);
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, umma_desc_sw128(kbase + ks * 32, 16, 1024), idS,
+                        (kb > 0 || ks > 0) ? 1u : 0u);
+            } else {             // A = Q block from shared memory
+              const uint32_t qb = smem_u32(qs + (kb - C::NQT) * (C::M * 128));
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024),
+                        idS, 1u);
+            }
             give();
           }
           if (!ok) break;
@@ -318,6 +400,31 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     const bool row_ok = t < x.n;
     const int qpos = x.P + t;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    {
+      // this row's first NQT * 64 query values into tensor memory (row =
+      // lane, bf16 pairs per column: the A-operand layout of the S MMA);
+      // rows past the last token are zero
+      const int tok = x.qo0 + t;
+      const bool in = tok < p.num_tokens;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
+#pragma unroll 1
+      for (int kb = 0; kb < C::NQT; ++kb) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = in ? __ldg(src + kb * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        tmem_st32(trow + C::Q_COL0 + kb * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qt_full);
+    }
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
@@ -388,12 +495,6 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       l_run += psum;
       tmem_st32(trow + s_col, pk);
       tmem_st_wait();
-      if (pre && st0 + 64 > x.P && (x.P & 15) != 0) {
-        // the producer zeroes the stale slab rows of the last prefix page
-        // (positions P .. next multiple of 16) in V_j before the PV MMA reads them
-        ok = mbar_wait(&san_bar, 0);
-        if (__any_sync(0xffffffffu, !ok)) break;
-      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
@@ -431,7 +532,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   // ------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == C::W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -450,6 +551,12 @@ static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStrea
 
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
   ExtK k{};
+  k.q = static_cast<const __nv_bfloat16*>(a.q);
+  k.k_slab = static_cast<const uint8_t*>(a.k_slab);
+  k.v_slab = static_cast<const uint8_t*>(a.v_slab);
+  k.k_ext = static_cast<const uint8_t*>(a.k_ext);
+  k.v_ext = static_cast<const uint8_t*>(a.v_ext);
+  k.num_tokens = a.num_tokens;
   k.qo_indptr = a.qo_indptr;
   k.prefix_lens = a.prefix_lens;
   k.block_table = a.block_table;
