@@ -47,7 +47,9 @@ struct ExtCfg {
   static constexpr int NQT = 4;                 // Q blocks held in tensor memory
   static constexpr int NQS = KB - NQT;          // Q blocks held in shared memory
   static constexpr int Q_BYTES = NQS * M * 128; // [NQS][128][64] bf16
-  static constexpr int SLOT = NK * 64 * 2;      // one ring slot: 64 keys x 64 columns (a K chunk or a V block)
+  static constexpr int CHUNK = NK * 64 * 2;     // 64 keys x 64 columns: a K chunk or a V block
+  static constexpr int CPS = D == 256 ? 4 : 2;  // chunks (column blocks) per ring slot
+  static constexpr int SLOT = CPS * CHUNK;      // one ring slot: CPS chunks side by side
   static constexpr int BAR_BYTES = 1024;
   // the rest of shared memory is a ring of slots; per tile KB K chunks and 4 V blocks pass through it
   static constexpr int NSLOT = (232448 - 1024 - Q_BYTES - BAR_BYTES) / SLOT;
@@ -66,7 +68,8 @@ struct ExtCfg {
   static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1) * 8 <= BAR_BYTES, "barrier space");
-  static_assert(NSLOT >= KB + 4, "a ring must hold one tile");
+  static_assert(NSLOT >= KB / CPS + 4 / CPS, "a ring must hold one tile");
+  static_assert(KB % CPS == 0 && 4 % CPS == 0, "slots hold whole groups of column blocks");
 };
 
 struct ExtK {
@@ -253,7 +256,8 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     };
     int e = 0;
     bool ok = true;
-    auto emit = [&](const TileSrc& ts, int blk, bool is_v) {
+    // one slot: column blocks blk0 .. blk0 + CPS - 1 (8 KB each)
+    auto emit = [&](const TileSrc& ts, int blk0, bool is_v) {
       if (e % C::NPW == pw) {
         const int sl = e % C::NSLOT;
         bool w = true;
@@ -266,12 +270,15 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
               int tx = 0;
 #pragma unroll
               for (int g = 0; g < 4; ++g)
-                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim) tx += 2048;
+                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim) tx += C::CPS * 2048;
               mbar_arrive_expect_tx(&full[sl], tx);
 #pragma unroll
-              for (int g = 0; g < 4; ++g)
-                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim)
-                  tma_load_3d(dst + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk, ts.row0[g], pol);
+              for (int h = 0; h < C::CPS; ++h)
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                  if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim)
+                    tma_load_3d(dst + h * C::CHUNK + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk0 + h,
+                                ts.row0[g], pol);
             }
             // groups without a page (or past the prefix) must read as zero: the slot holds older data
             const uint8_t* base = is_v ? p.v_slab : p.k_slab;
@@ -281,21 +288,25 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
               const bool tma = g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim;
               if (tma) continue;
               any_cp = true;
-              // 16 rows x 8 units: lane copies rows lane / 8 + 4 i, unit lane % 8
+              // 16 rows x 8 units per block: lane copies rows lane / 8 + 4 i, unit lane % 8
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
-                const bool v = ts.row0[g] >= 0 && r < ts.lim;
-                const uint8_t* src = base + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + blk * 64) * 2 + (lane & 7) * 16 : 0);
-                cp_async16_zfill(dst + sw128(r, lane & 7), src, v, pol);
-              }
+              for (int h = 0; h < C::CPS; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
+                  const bool v = ts.row0[g] >= 0 && r < ts.lim;
+                  const uint8_t* src =
+                      base + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + (blk0 + h) * 64) * 2 + (lane & 7) * 16 : 0);
+                  cp_async16_zfill(dst + h * C::CHUNK + sw128(r, lane & 7), src, v, pol);
+                }
             }
             if (any_cp) cp_async_mbar_arrive(&full[sl]);
             else if (lane == 0) mbar_arrive_n(&full[sl], 32);
           } else {
             if (lane == 0) {
               mbar_arrive_expect_tx(&full[sl], C::SLOT);
-              tma_load_4d(dst, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, ts.tok0, pol);
+              for (int h = 0; h < C::CPS; ++h)
+                tma_load_4d(dst + h * C::CHUNK, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk0 + h, x.h, ts.tok0, pol);
               mbar_arrive_n(&full[sl], 32);
             }
           }
@@ -310,10 +321,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         const int pid = pid_next;
         pid_next = load_pid(t + 1);   // a tile ahead
         src_cur = tile_src(t, pid);
-        for (int kb = 0; ok && kb < C::KB; ++kb) emit(src_cur, kb, false);
+        for (int kb = 0; ok && kb < C::KB; kb += C::CPS) emit(src_cur, kb, false);
       }
       if (t >= 1)
-        for (int i4 = 0; ok && i4 < 4; ++i4) emit(src_prev, x.ds * 4 + i4, true);
+        for (int i4 = 0; ok && i4 < 4; i4 += C::CPS) emit(src_prev, x.ds * 4 + i4, true);
       src_prev = src_cur;
     }
     if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);
-      const uint32_t idO = umma_idesc_bf16(C::M, 64, true);
+      const uint32_t idO = umma_idesc_bf16(C::M, 64 * C::CPS, true);   // the V blocks of a slot, LBO = CHUNK
       bool ok = mbar_wait(q_full, 0) && mbar_wait(qt_full, 0);
       tc_fence_after();
       int e = 0;
@@ -349,20 +360,25 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
           if (t >= 2) ok = mbar_wait(&o_bar[t & 1], ((t - 2) >> 1) & 1);   // PV_{t-2} has read P from this buffer
           tc_fence_after();
           const uint32_t s_tmem = tmem + C::S_COL0 + sb * 64;
-          for (int kb = 0; ok && kb < C::KB; ++kb) {
-            const uint32_t kbase = take();
+          for (int kp = 0; ok && kp < C::KB; kp += C::CPS) {
+            const uint32_t sbase = take();   // K chunks kp .. kp + CPS - 1
             if (!ok) break;
-            if (kb < C::NQT) {   // A = Q block from tensor memory
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, umma_desc_sw128(kbase + ks * 32, 16, 1024), idS,
-                        (kb > 0 || ks > 0) ? 1u : 0u);
-            } else {             // A = Q block from shared memory
-              const uint32_t qb = smem_u32(qs + (kb - C::NQT) * (C::M * 128));
+            for (int h = 0; h < C::CPS; ++h) {
+              const int kb = kp + h;
+              const uint32_t kbase = sbase + h * C::CHUNK;
+              if (kb < C::NQT) {   // A = Q block from tensor memory
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024),
-                        idS, 1u);
+                for (int ks = 0; ks < 4; ++ks)
+                  umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, umma_desc_sw128(kbase + ks * 32, 16, 1024),
+                          idS, (kb > 0 || ks > 0) ? 1u : 0u);
+              } else {             // A = Q block from shared memory
+                const uint32_t qb = smem_u32(qs + (kb - C::NQT) * (C::M * 128));
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                  umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024),
+                          idS, 1u);
+              }
             }
             give();
           }
@@ -374,13 +390,13 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
           ok = ok && mbar_wait(&p_full[sb], (i >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          for (int i4 = 0; ok && i4 < 4; ++i4) {
-            const uint32_t vbase = take();   // V block i4: 64 keys x 64 output columns, MN-major
+          for (int i4 = 0; ok && i4 < 4; i4 += C::CPS) {
+            const uint32_t vbase = take();   // V blocks i4 ..: 64 keys x 64 CPS output columns, MN-major
             if (!ok) break;
 #pragma unroll
             for (int ks = 0; ks < C::NK / 16; ++ks)
               umma_ts(tmem + i4 * 64, tmem + C::S_COL0 + sb * 64 + ks * 8,
-                      umma_desc_sw128(vbase + ks * 2048, 8192, 1024), idO, (i > 0 || ks > 0) ? 1u : 0u);
+                      umma_desc_sw128(vbase + ks * 2048, C::CHUNK, 1024), idO, (i > 0 || ks > 0) ? 1u : 0u);
             give();
           }
           umma_commit(&o_bar[i & 1]);   // PV i completes phase i / 2 of o_bar[i & 1]
