@@ -455,27 +455,25 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       tmem_ld_wait();
       const int st0 = x.start(j);
       const bool pre = x.prefix(j);
+      // raw scores of this row's visible keys (columns [clo, chi]: one
+      // interval per row from the causal, window and prefix-end limits),
+      // -inf elsewhere; the scale is applied inside the exponent below
       float sv[64];
-      float mt = -INFINITY;
-      // this row's visible keys in this tile are the columns [clo, chi]: one
-      // interval per row (causal, window, prefix end), two compares per key
       const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
       const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.P - 1) : qpos);
       const int clo = klo - st0, chi = khi - st0;
       const float sc = p.scale_log2;
       if (__all_sync(0xffffffffu, clo <= 0 && chi >= 63)) {   // the whole tile is visible to the warp's rows
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          sv[c] = __uint_as_float(sr[c >> 5][c & 31]) * sc;
-          mt = fmaxf(mt, sv[c]);
-        }
+        for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(sr[c >> 5][c & 31]);
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sr[c >> 5][c & 31]) * sc : -INFINITY;
-          mt = fmaxf(mt, sv[c]);
-        }
+        for (int c = 0; c < 64; ++c) sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sr[c >> 5][c & 31]) : -INFINITY;
       }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + 8.0f;   // rescale only when the max grows by more than 2^8
       if (__any_sync(0xffffffffu, need && m_run > -INFINITY) && j > 0) {
@@ -499,16 +497,18 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         m_run = m_new;
       }
       uint32_t pk[32];
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // a row with no visible key so far has m_run = -inf and only -inf scores: exponent base 0 gives 0
+      const float mb = (m_run > -INFINITY) ? m_run : 0.f;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = (m_run > -INFINITY) ? ex2(sv[2 * c] - m_run) : 0.f;
-        const float p1 = (m_run > -INFINITY) ? ex2(sv[2 * c + 1] - m_run) : 0.f;
+        const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
+        const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
         pk[c] = pack_bf16x2(p0, p1);
         // the denominator sums the bf16-rounded weights the PV MMA uses
-        psum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+        ps[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
       }
-      l_run += psum;
+      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       tmem_st32(trow + s_col, pk);
       tmem_st_wait();
       tc_fence_before();
