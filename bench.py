@@ -559,7 +559,10 @@ def prefill_measure(args, dev):
             "roofline": {"kernel": "extend_kernel (tcgen05 chunked prefill)", "bound": "tensor",
                          "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                          "frac": round(achieved / bf16, 3), "peak_source": src + " (dense bf16 burst)",
-                         "traffic": None, "per_layer": per_layer},
+                         "traffic": profiled_traffic("extend_chunked_prefill",
+                                                     source_digest("fa_extend.cu", "fa_ptx.cuh")),
+                         "algorithmic_flop_per_launch": round(step.total_flops / (step.nchunks * nl)),
+                         "per_layer": per_layer},
             "gpu_launches_per_prefill": step.launches(), "graph": g_plain is not None}
 
 
@@ -661,7 +664,7 @@ def cpu_baseline(name, seconds):
         per = -(-pool.units // pool.procs)
         nb, t = pool.run(per)
         reps = 1
-        while t < seconds / 4 and reps < 8:
+        while t < seconds * 2 / 3 and reps < 64:
             b2, t2 = pool.run(per)
             nb, t, reps = nb + b2, t + t2, reps + 1
     finally:
