@@ -314,7 +314,8 @@ __device__ void merge_unit(const DecK& p, int u, const Unit& x, int nh, int head
           acc[i].w += w * o.w;
         }
       }
-      named_bar_sync(1, 128);   // every thread is done with this batch's rows
+      fence_proxy_async_smem();   // these generic reads before the next batch's bulk copies
+      named_bar_sync(1, 128);     // every thread is done with this batch's rows
       if (b0 + NB < nct && tid == 0) stage_batch(b0 + NB, batch + 1);
     }
   }
@@ -625,7 +626,10 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
     const bool hv = gid < nh;
 
     // queries of this segment: Q^T fragments (B operand), zero for padded heads
-    if (!mbar_wait(qfull, j & 1) && lane == 0) {
+    // every wait below is made warp-uniform (and the warp reconverged) by a
+    // vote, since ldmatrix and mma.sync need all 32 lanes together
+    const bool qok = __all_sync(0xffffffffu, mbar_wait(qfull, j & 1));
+    if (!qok && lane == 0) {
       abort_flag = 1;
       atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     }
@@ -649,6 +653,11 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
         }
       }
     }
+    // qbuf is refilled by a bulk copy (async proxy) once every warp has
+    // arrived: each thread's generic reads of it are ordered before that
+    // write by a proxy fence, which also waits for loads still in flight
+    // (the fragments are not used before the arrive)
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(qempty);
 
@@ -664,7 +673,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
       const uint8_t* ks = smem + st * C::STAGE_KV;
       const uint8_t* vs = ks + C::NT * C::TILE_BYTES;
       const float* scl = reinterpret_cast<const float*>(smem + C::OFF_SC + st * C::SC_BYTES);
-      const bool ok = mbar_wait(&full[st], (gi / C::NSTAGE) & 1);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (gi / C::NSTAGE) & 1));
       if (!ok && lane == 0) {
         abort_flag = 1;
         atomicOr(p.err, FA_DEV_ERR_TIMEOUT);

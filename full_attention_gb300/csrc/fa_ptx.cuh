@@ -70,14 +70,14 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
-// Order this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA / tensor core) accesses of the same bytes.
 // Order this thread's generic-proxy view of global memory (e.g. data made
 // visible by an acquire) before its later async-proxy (bulk copy) reads.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA / tensor core) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -207,7 +207,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Named barrier over `nthreads` threads (whole warps).  bar.sync is the
+// warp-aligned form: a warp must reach it with all lanes together, and a warp
+// that arrives split (after a divergent branch or a per-lane spin) is counted
+// once per fragment, which releases the barrier before the other warps are
+// there.  The compiler does not treat the inline asm as convergent, so the
+// warp is reconverged first.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 

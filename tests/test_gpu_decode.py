@@ -116,6 +116,30 @@ def test_determinism_and_graph_replay():
         assert torch.equal(a, b) and torch.equal(la, lb)
 
 
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("shape", ["d256_g8", "d256_g8_one_kv", "d512_g8"])
+def test_repeated_decodes_are_bit_identical(shape, kv_dtype):
+    """Alternating layers with many short segments per CTA (one-tile and
+    three-tile units next to long ones) stress the per-segment hand-off of the
+    queries: every repeat must equal the first run bit for bit."""
+    if shape == "d256_g8":
+        layers, lens = [lay(W.SLIDING, 256, 16, 2, 33), lay(W.FULL, 256, 16, 2)], [3, 33, 34, 49, 150, 700]
+    elif shape == "d256_g8_one_kv":
+        layers, lens = [lay(W.FULL, 256, 8, 1), lay(W.SLIDING, 256, 8, 1, 64)], [1, 17, 300, 1000, 5, 64, 65, 2049]
+    else:
+        layers, lens = [lay(W.SLIDING, 512, 8, 1, 40), lay(W.FULL, 512, 8, 1)], [3, 33, 34, 49, 150, 700]
+    case = DecodeCase(layers, lens, 16, kv_dtype, seed=22)
+    case.store_current()
+    ref = [case.decode(i) for i in range(len(layers))]
+    bad = 0
+    for _ in range(60):
+        for i in range(len(layers)):
+            o, lse = case.decode(i)
+            bad += not (torch.equal(o, ref[i][0]) and torch.equal(lse, ref[i][1]))
+    assert bad == 0
+    assert case.fa.device_error() == 0
+
+
 def test_bad_page_id_sets_device_error():
     """A visible block-table entry outside the pool is skipped (the TMA box
     then lies outside the tensor and reads zeros) and reported."""
