@@ -17,14 +17,15 @@
 // the first 256 columns of Q as bf16 pairs [384, 512), so S = Q K^T reads
 // that part of Q from tensor memory and only the rest (head_dim 512) from
 // shared memory; the freed shared memory deepens the K/V ring.  Roles:
-//   warp 0      TMA producer: the shared-memory part of Q once (4-D map,
+//   warps 0-3   producers: the shared-memory part of Q once (4-D map,
 //               rows = (token, head)); per 64-key tile the K tile in
 //               64-column chunks and the V tile of this CTA's output slice,
-//               from slab pages or from k_ext / v_ext;
-//   warp 1      MMA issuer: S_j = Q K_j^T (tcgen05.mma, M=128, N=64, fp32 in
-//               TMEM, double buffered), then O += P_{j-1} V_{j-1} with P read
-//               from tensor memory and V as an MN-major operand (N=256);
-//   warps 2-5   softmax: one query row per thread; first copy the row's
+//               from slab pages or from k_ext / v_ext, slot e by warp e % 4;
+//   warp 4      MMA issuer (the whole warp walks the schedule, one elected
+//               lane issues): S_j = Q K_j^T (tcgen05.mma, M=128, N=64, fp32
+//               in TMEM, double buffered), then O += P_{j-1} V_{j-1} with P
+//               read from tensor memory and V as an MN-major operand;
+//   warps 5-8   softmax: one query row per thread; first copy the row's
 //               leading 256 Q values into tensor memory; per tile load S, mask,
 //               online softmax in the log2 domain, write P (bf16) back into the
 //               S buffer; rescale O in TMEM only when the running max grows by
@@ -42,9 +43,16 @@ template <int D>
 struct ExtCfg {
   static constexpr int M = 128;                 // query rows per CTA
   static constexpr int NK = 64;                 // keys per tile
-  static constexpr int DS = 256;                // output columns per CTA
+  // Output columns per CTA.  Tensor memory (512 columns) holds O (DS
+  // columns), two 64-column S/P buffers and as many 64-column blocks of Q
+  // (bf16 pairs, 32 columns each) as fit; the rest of Q stays in shared
+  // memory.  head_dim 512 uses two CTAs per 128-row block (each recomputes S);
+  // four CTAs with 128 columns each would hold all of Q in tensor memory but
+  // doubles the S work again, which costs more than it saves.
+  static constexpr int DS = 256;
+  static constexpr int NVB = DS / 64;           // 64-column V blocks per tile
   static constexpr int KB = D / 64;             // 64-column blocks of head_dim
-  static constexpr int NQT = 4;                 // Q blocks held in tensor memory
+  static constexpr int NQT = (512 - DS - 128) / 32 < KB ? (512 - DS - 128) / 32 : KB;   // Q blocks in tensor memory
   static constexpr int NQS = KB - NQT;          // Q blocks held in shared memory
   static constexpr int Q_BYTES = NQS * M * 128; // [NQS][128][64] bf16
   static constexpr int CHUNK = NK * 64 * 2;     // 64 keys x 64 columns: a K chunk or a V block
@@ -60,16 +68,17 @@ struct ExtCfg {
   static constexpr int NPW = 4;                 // producer warps
   static constexpr int W_MMA = NPW;             // the MMA warp; the softmax warps follow it
   static constexpr int NTHR = (NPW + 1 + 4) * 32;
-  // tensor memory columns: O [0, 256), S/P buffers [256, 320) and [320, 384),
-  // Q blocks 0..NQT-1 [384, 512) (32 columns of bf16 pairs each)
+  // tensor memory columns: O [0, DS), S/P buffers [DS, DS + 64) and
+  // [DS + 64, DS + 128), Q blocks 0..NQT-1 [DS + 128, 512) (32 columns of
+  // bf16 pairs each)
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL0 = 256;
-  static constexpr uint32_t Q_COL0 = 384;
+  static constexpr uint32_t S_COL0 = DS;
+  static constexpr uint32_t Q_COL0 = DS + 128;
   static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1) * 8 <= BAR_BYTES, "barrier space");
-  static_assert(NSLOT >= KB / CPS + 4 / CPS, "a ring must hold one tile");
-  static_assert(KB % CPS == 0 && 4 % CPS == 0, "slots hold whole groups of column blocks");
+  static_assert(NSLOT >= KB / CPS + NVB / CPS, "a ring must hold one tile");
+  static_assert(KB % CPS == 0 && NVB % CPS == 0, "slots hold whole groups of column blocks");
 };
 
 struct ExtK {
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         for (int kb = 0; ok && kb < C::KB; kb += C::CPS) emit(src_cur, kb, false);
       }
       if (t >= 1)
-        for (int i4 = 0; ok && i4 < 4; i4 += C::CPS) emit(src_prev, x.ds * 4 + i4, true);
+        for (int i4 = 0; ok && i4 < C::NVB; i4 += C::CPS) emit(src_prev, x.ds * C::NVB + i4, true);
       src_prev = src_cur;
     }
     if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
@@ -337,32 +346,36 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     if (threadIdx.x == 0 && !mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
   } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);
-      const uint32_t idO = umma_idesc_bf16(C::M, 64 * C::CPS, true);   // the V blocks of a slot, LBO = CHUNK
-      bool ok = mbar_wait(q_full, 0) && mbar_wait(qt_full, 0);
+    // The whole warp walks the schedule and waits on the barriers, so slot
+    // addresses and descriptors are warp-uniform; one elected lane (always
+    // the same one) issues the MMAs and the commits that track them.
+    const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);
+    const uint32_t idO = umma_idesc_bf16(C::M, 64 * C::CPS, true);   // the V blocks of a slot, LBO = CHUNK
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0) && mbar_wait(qt_full, 0));
+    tc_fence_after();
+    int e = 0;
+    auto take = [&]() -> uint32_t {   // wait for the next ring slot, return its address
+      const int sl = e % C::NSLOT;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[sl], (e / C::NSLOT) & 1));
+      fence_proxy_async_smem();   // the cp.async writes, seen through the barrier, for the MMA's reads
       tc_fence_after();
-      int e = 0;
-      auto take = [&]() -> uint32_t {   // wait for the next ring slot, return its address
-        const int sl = e % C::NSLOT;
-        ok = ok && mbar_wait(&full[sl], (e / C::NSLOT) & 1);
-        fence_proxy_async_smem();   // the cp.async writes, seen through the barrier, for the MMA's reads
+      return smem_u32(ring + sl * C::SLOT);
+    };
+    auto give = [&]() {   // release the slot once the MMAs reading it complete
+      if (elect_one()) umma_commit(&empty[e % C::NSLOT]);
+      __syncwarp();
+      ++e;
+    };
+    for (int t = 0; ok && t <= nt; ++t) {
+      if (t < nt) {
+        const int sb = t & 1;
+        if (t >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&o_bar[t & 1], ((t - 2) >> 1) & 1));   // PV_{t-2} has read P
         tc_fence_after();
-        return smem_u32(ring + sl * C::SLOT);
-      };
-      auto give = [&]() {   // release the slot once the MMAs reading it complete
-        umma_commit(&empty[e % C::NSLOT]);
-        ++e;
-      };
-      for (int t = 0; ok && t <= nt; ++t) {
-        if (t < nt) {
-          const int sb = t & 1;
-          if (t >= 2) ok = mbar_wait(&o_bar[t & 1], ((t - 2) >> 1) & 1);   // PV_{t-2} has read P from this buffer
-          tc_fence_after();
-          const uint32_t s_tmem = tmem + C::S_COL0 + sb * 64;
-          for (int kp = 0; ok && kp < C::KB; kp += C::CPS) {
-            const uint32_t sbase = take();   // K chunks kp .. kp + CPS - 1
-            if (!ok) break;
+        const uint32_t s_tmem = tmem + C::S_COL0 + sb * 64;
+        for (int kp = 0; ok && kp < C::KB; kp += C::CPS) {
+          const uint32_t sbase = take();   // K chunks kp .. kp + CPS - 1
+          if (!ok) break;
+          if (elect_one()) {
 #pragma unroll
             for (int h = 0; h < C::CPS; ++h) {
               const int kb = kp + h;
@@ -380,33 +393,40 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
                           idS, 1u);
               }
             }
-            give();
           }
-          if (!ok) break;
-          umma_commit(&s_full[sb]);
+          __syncwarp();
+          give();
         }
-        if (t >= 1) {
-          const int i = t - 1, sb = i & 1;
-          ok = ok && mbar_wait(&p_full[sb], (i >> 1) & 1);
+        if (!ok) break;
+        if (elect_one()) umma_commit(&s_full[sb]);
+        __syncwarp();
+      }
+      if (t >= 1) {
+        const int i = t - 1, sb = i & 1;
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&p_full[sb], (i >> 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        for (int i4 = 0; ok && i4 < C::NVB; i4 += C::CPS) {
+          const uint32_t vbase = take();   // V blocks i4 ..: 64 keys x 64 CPS output columns, MN-major
           if (!ok) break;
-          tc_fence_after();
-          for (int i4 = 0; ok && i4 < 4; i4 += C::CPS) {
-            const uint32_t vbase = take();   // V blocks i4 ..: 64 keys x 64 CPS output columns, MN-major
-            if (!ok) break;
+          if (elect_one()) {
 #pragma unroll
             for (int ks = 0; ks < C::NK / 16; ++ks)
               umma_ts(tmem + i4 * 64, tmem + C::S_COL0 + sb * 64 + ks * 8,
                       umma_desc_sw128(vbase + ks * 2048, C::CHUNK, 1024), idO, (i > 0 || ks > 0) ? 1u : 0u);
-            give();
           }
-          umma_commit(&o_bar[i & 1]);   // PV i completes phase i / 2 of o_bar[i & 1]
+          __syncwarp();
+          give();
         }
+        if (elect_one()) umma_commit(&o_bar[i & 1]);   // PV i completes phase i / 2 of o_bar[i & 1]
+        __syncwarp();
       }
-      if (!ok) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-      // every MMA this thread issued has finished before tensor memory is freed
-      umma_commit(&done_bar);
-      if (!mbar_wait(&done_bar, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     }
+    if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    // every MMA the elected lane issued has finished before tensor memory is freed
+    if (elect_one()) umma_commit(&done_bar);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(&done_bar, 0)) && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
   } else {
     // ------------------------------------------------------------- softmax
     const int quarter = warp & 3;
@@ -592,7 +612,7 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
   k.max_pages_per_seq = a.max_pages_per_seq;
   k.max_q_len = a.max_q_len;
   k.max_prefix_len = a.max_prefix_len;
-  k.dslices = a.D / 256;
+  k.dslices = a.D / ExtCfg<256>::DS;
   k.early_metadata = a.early_metadata;
   k.scale_log2 = a.sm_scale * 1.4426950408889634f;
   if (a.D == 256) return launch_extend_t<256>(a, k, s);

@@ -259,6 +259,17 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// One lane of a converged warp (the lowest active one) gets true.  Issuing
+// tcgen05 work from a converged warp through this keeps slot addresses and
+// descriptors warp-uniform, so they stay in the uniform datapath; computing
+// them inside a lane-0-only branch costs about a hundred cycles per MMA.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
 // Arrive once on `bar` when every tcgen05 operation this thread issued has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
