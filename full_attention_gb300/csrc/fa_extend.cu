@@ -229,14 +229,25 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       prefetch_tmap(&tm_vx);
     }
     const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
-    // page ids of tile j's 4 row groups, lanes 0-3 (-1: not a prefix row; -2: bad page id)
-    auto load_pid = [&](int j) -> int {
-      int pid = -1;
+    // Page of row group `lane` (lanes 0-3) of tile j and the group's offset in
+    // it (pid -1: not a prefix row).  Looked up a tile ahead; the id is
+    // checked where it is used.  Every producer warp resolves every tile, so
+    // this per-tile work is kept short: one division per lane, done here,
+    // and the lanes of a tile's four groups work in parallel.
+    struct PageRef {
+      int pid, off;
+    };
+    auto load_pid = [&](int j) -> PageRef {
+      PageRef r{-1, 0};
       if (j < nt && x.prefix(j) && lane < 4) {
         const int pos = x.start(j) + 16 * lane;   // a 16-row group lies in one page
-        if (pos < x.P) pid = __ldg(bt + pos / p.page_size);   // checked where it is used, a tile later
+        if (pos < x.P) {
+          const int q = pos / p.page_size;
+          r.off = pos - q * p.page_size;
+          r.pid = ld_nc_early(bt + q);
+        }
       }
-      return pid;
+      return r;
     };
     struct TileSrc {
       int row0[4];   // slab row of each 16-row group (prefix tiles), -1: no page
@@ -245,22 +256,24 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       bool prefix;
       int tok0;      // chunk tiles: first token row in k_ext / v_ext
     };
-    auto tile_src = [&](int j, int pid) {
+    auto tile_src = [&](int j, PageRef pr) {
       TileSrc ts;
       const int st0 = x.start(j);
       ts.prefix = x.prefix(j);
       ts.lim = ts.prefix ? x.P - st0 : x.n - (st0 - x.P);
       ts.bgroup = (ts.prefix && ts.lim < 64 && (ts.lim & 15) != 0) ? (ts.lim >> 4) : -1;
       ts.tok0 = x.qo0 + st0 - x.P;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        int pg = __shfl_sync(0xffffffffu, pid, g);
-        if (ts.prefix && 16 * g < ts.lim && (pg < 0 || pg >= p.num_pages)) {   // a bad page id reads as zeros
-          if (pw == 0 && lane == 0) atomicOr(p.err, FA_DEV_ERR_PAGE);
-          pg = -1;
+      // lane g < 4 resolves group g's slab row; a bad page id reads as zeros
+      int r0 = -1;
+      if (lane < 4 && ts.prefix && 16 * lane < ts.lim) {
+        if (pr.pid < 0 || pr.pid >= p.num_pages) {
+          if (pw == 0) atomicOr(p.err, FA_DEV_ERR_PAGE);
+        } else {
+          r0 = (pr.pid * p.Hkv + x.h) * p.page_size + pr.off;
         }
-        ts.row0[g] = pg >= 0 ? (pg * p.Hkv + x.h) * p.page_size + (st0 + 16 * g) % p.page_size : -1;
       }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) ts.row0[g] = __shfl_sync(0xffffffffu, r0, g);
       return ts;
     };
     int e = 0;
@@ -323,11 +336,11 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       }
       ++e;
     };
-    int pid_next = load_pid(0);
+    PageRef pid_next = load_pid(0);
     TileSrc src_cur{}, src_prev{};
     for (int t = 0; ok && t <= nt; ++t) {
       if (t < nt) {
-        const int pid = pid_next;
+        const PageRef pid = pid_next;
         pid_next = load_pid(t + 1);   // a tile ahead
         src_cur = tile_src(t, pid);
         for (int kb = 0; ok && kb < C::KB; kb += C::CPS) emit(src_cur, kb, false);

@@ -115,6 +115,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// 32-bit read-only global load issued exactly here: the compiler keeps a
+// volatile asm in place, so a value loaded a step ahead of its use really is
+// in flight meanwhile (a plain load may be sunk next to its first use).
+__device__ __forceinline__ int ld_nc_early(const int32_t* ptr) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+
 // Hint: bring `bytes` (a multiple of 16, 16-byte aligned source) into L2.
 // No data reaches the SM and nothing is ordered with it, so it may be issued
 // before the data is known to be final.
