@@ -25,7 +25,8 @@
 //               lane issues): S_j = Q K_j^T (tcgen05.mma, M=128, N=64, fp32
 //               in TMEM, double buffered), then O += P_{j-1} V_{j-1} with P
 //               read from tensor memory and V as an MN-major operand;
-//   warps 5-8   softmax: one query row per thread; first copy the row's
+//   warps 5-12  softmax: two warps per row quarter, each thread one query
+//               row and half of each tile's 64 columns; first copy the row's
 //               leading 256 Q values into tensor memory; per tile load S, mask,
 //               online softmax in the log2 domain, write P (bf16) back into the
 //               S buffer; rescale O in TMEM only when the running max grows by
@@ -67,7 +68,8 @@ struct ExtCfg {
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   static constexpr int NPW = 4;                 // producer warps
   static constexpr int W_MMA = NPW;             // the MMA warp; the softmax warps follow it
-  static constexpr int NTHR = (NPW + 1 + 4) * 32;
+  static constexpr int NSMX = 8;                // softmax warps: two per tensor-memory lane quarter
+  static constexpr int NTHR = (NPW + 1 + NSMX) * 32;
   // tensor memory columns: O [0, DS), S/P buffers [DS, DS + 64) and
   // [DS + 64, DS + 128), Q blocks 0..NQT-1 [DS + 128, 512) (32 columns of
   // bf16 pairs each)
@@ -76,7 +78,7 @@ struct ExtCfg {
   static constexpr uint32_t Q_COL0 = DS + 128;
   static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1) * 8 <= BAR_BYTES, "barrier space");
+  static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 1) * 8 <= BAR_BYTES, "barrier space");
   static_assert(NSLOT >= KB / CPS + NVB / CPS, "a ring must hold one tile");
   static_assert(KB % CPS == 0 && NVB % CPS == 0, "slots hold whole groups of column blocks");
 };
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_bar = p_full + 2;
   uint64_t* qt_full = o_bar + 2;        // the softmax warps have put Q into tensor memory
-  __shared__ uint32_t tmem_slot;
-  __shared__ uint64_t done_bar;
+  uint64_t& done_bar = qt_full[1];      // every MMA has completed (before tensor memory is freed)
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(qt_full + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!p.early_metadata) griddep_wait();
@@ -185,11 +187,11 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], C::NSMX);
     }
     mbar_init(&o_bar[0], 1);
     mbar_init(&o_bar[1], 1);
-    mbar_init(qt_full, 4);
+    mbar_init(qt_full, C::NSMX);
     mbar_init(&done_bar, 1);
     fence_mbar_init();
   }
@@ -442,6 +444,18 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     if (!__all_sync(0xffffffffu, mbar_wait(&done_bar, 0)) && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
   } else {
     // ------------------------------------------------------------- softmax
+    // Two warps per row quarter (tensor-memory lane access follows warp % 4):
+    // the first four take columns [0, 32) of each 64-key tile, the other four
+    // columns [32, 64).  The two halves of a row exchange their tile maxima
+    // through shared memory (double buffered by tile parity) once per tile,
+    // each rounded up to bf16 so that both halves take the same value (any
+    // common base gives the same softmax); that barrier ANDs each warp's wait
+    // result, so all eight leave the loop together.  Each half keeps its share
+    // of the denominator; the shares meet once in the epilogue, through the
+    // ring, which is idle by then.
+    __shared__ __nv_bfloat16 sm_mx[2][2][C::M];   // [tile parity][half][row]
+    constexpr int SMX_BAR = 2, SMX_THREADS = C::NSMX * 32;
+    const int half = (warp - (C::W_MMA + 1)) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;   // query row = tensor-memory lane
     const int tl = r / p.g, hj = r % p.g;
@@ -451,13 +465,13 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     {
       // this row's first NQT * 64 query values into tensor memory (row =
-      // lane, bf16 pairs per column: the A-operand layout of the S MMA);
-      // rows past the last token are zero
+      // lane, bf16 pairs per column: the A-operand layout of the S MMA),
+      // half h copying blocks h, h + 2, ...; rows past the last token are zero
       const int tok = x.qo0 + t;
       const bool in = tok < p.num_tokens;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
 #pragma unroll 1
-      for (int kb = 0; kb < C::NQT; ++kb) {
+      for (int kb = half; kb < C::NQT; kb += 2) {
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -474,67 +488,80 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(qt_full);
     }
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
+    const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
+    const float sc = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;   // l_run: this half's share of the denominator
+    bool ok = true, bad = false;
+    constexpr int OH = C::DS / 2;            // O columns this half rescales and writes
     for (int j = 0; j < nt; ++j) {
       const int sb = j & 1;
       const uint32_t s_col = C::S_COL0 + sb * 64;
-      ok = mbar_wait(&s_full[sb], (j >> 1) & 1);
-      if (__any_sync(0xffffffffu, !ok)) break;
-      tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(trow + s_col, sr[0]);
-      tmem_ld32(trow + s_col + 32, sr[1]);
-      tmem_ld_wait();
-      const int st0 = x.start(j);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1));
       const bool pre = x.prefix(j);
-      // raw scores of this row's visible keys (columns [clo, chi]: one
-      // interval per row from the causal, window and prefix-end limits),
-      // -inf elsewhere; the scale is applied inside the exponent below
-      float sv[64];
-      const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
-      const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.P - 1) : qpos);
-      const int clo = klo - st0, chi = khi - st0;
-      const float sc = p.scale_log2;
-      if (__all_sync(0xffffffffu, clo <= 0 && chi >= 63)) {   // the whole tile is visible to the warp's rows
+      const int st0 = x.start(j) + 32 * half;   // key of this half's first column
+      // raw scores of this row's visible keys (one interval [clo, chi] per
+      // row from the causal, window and prefix-end limits), -inf elsewhere;
+      // the scale is applied inside the exponent below
+      float sv[32];
+      float mt = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld32(trow + s_col + 32 * half, sr);
+        tmem_ld_wait();
+        const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.P - 1) : qpos);
+        const int clo = klo - st0, chi = khi - st0;
+        if (__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {   // all 32 columns visible to the warp's rows
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(sr[c >> 5][c & 31]);
-      } else {
+          for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(sr[c]);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sr[c >> 5][c & 31]) : -INFINITY;
+          for (int c = 0; c < 32; ++c) sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sr[c]) : -INFINITY;
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+        const __nv_bfloat16 mr = __float2bfloat16_ru(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc);
+        sm_mx[sb][half][r] = mr;
+        mt = __bfloat162float(mr);
       }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
-#pragma unroll
-      for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+      // every warp has loaded its S half (so P may now overwrite the S
+      // buffer) and published its maximum
+      ok = named_bar_and(SMX_BAR, SMX_THREADS, got && !bad);
+      if (!ok) break;
+      mt = fmaxf(mt, __bfloat162float(sm_mx[sb][half ^ 1][r]));
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + 8.0f;   // rescale only when the max grows by more than 2^8
       if (__any_sync(0xffffffffu, need && m_run > -INFINITY) && j > 0) {
-        ok = mbar_wait(&o_bar[(j - 1) & 1], ((j - 1) >> 1) & 1);   // PV_{j-1} has finished writing O
-        if (__any_sync(0xffffffffu, !ok)) break;
-        tc_fence_after();
-        const float f = (need && m_run > -INFINITY) ? ex2(m_run - m_new) : 1.0f;
+        // PV_{j-1} has finished writing O; this half rescales its O columns
+        if (__all_sync(0xffffffffu, mbar_wait(&o_bar[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+          tc_fence_after();
+          const float f = (need && m_run > -INFINITY) ? ex2(m_run - m_new) : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < C::DS; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(trow + c, o);
-          tmem_ld_wait();
+          for (int c = half * OH; c < (half + 1) * OH; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(trow + c, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-          tmem_st32(trow + c, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(trow + c, o);
+          }
+          tmem_st_wait();
+        } else {
+          bad = true;   // leaves the loop at the next tile's barrier
+          if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
         }
-        tmem_st_wait();
       }
       if (need) {
         l_run = (m_run > -INFINITY) ? l_run * ex2(m_run - m_new) : 0.f;
         m_run = m_new;
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
       // a row with no visible key so far has m_run = -inf and only -inf scores: exponent base 0 gives 0
       const float mb = (m_run > -INFINITY) ? m_run : 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 16; ++c) {
         const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
         const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
         pk[c] = pack_bf16x2(p0, p1);
@@ -542,23 +569,29 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         ps[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
       }
       l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tmem_st32(trow + s_col, pk);
+      tmem_st16(trow + s_col + 16 * half, pk);   // P of keys [32 half, 32 half + 32): 16 columns of bf16 pairs
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && nt > 0) ok = mbar_wait(&o_bar[(nt - 1) & 1], ((nt - 1) >> 1) & 1);
-    if (__any_sync(0xffffffffu, !ok)) {
+    bool fin = ok;
+    if (fin && nt > 0) fin = __all_sync(0xffffffffu, mbar_wait(&o_bar[(nt - 1) & 1], ((nt - 1) >> 1) & 1));
+    // every MMA has completed, so every ring slot was consumed: the ring is idle
+    float* sm_l = reinterpret_cast<float*>(ring);   // [half][row]
+    if (fin) sm_l[half * C::M + r] = l_run;
+    fin = named_bar_and(SMX_BAR, SMX_THREADS, fin);
+    const float l_tot = fin ? l_run + sm_l[(half ^ 1) * C::M + r] : 0.f;
+    if (!fin) {
       if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     } else {
       tc_fence_after();
-      const float inv = (l_run > 0.f) ? 1.0f / l_run : 0.f;
+      const float inv = (l_tot > 0.f) ? 1.0f / l_tot : 0.f;
       __nv_bfloat16* orow =
           p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS;
 #pragma unroll 1
-      for (int c = 0; c < C::DS; c += 32) {
+      for (int c = half * OH; c < (half + 1) * OH; c += 32) {
         uint32_t o[32];
         tmem_ld32(trow + c, o);
         tmem_ld_wait();
@@ -572,9 +605,9 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
             reinterpret_cast<uint4*>(orow + c)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
         }
       }
-      if (row_ok && x.ds == 0 && p.lse)
+      if (row_ok && half == 0 && x.ds == 0 && p.lse)
         p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
-            (m_run > -INFINITY && l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            (m_run > -INFINITY && l_tot > 0.f) ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
