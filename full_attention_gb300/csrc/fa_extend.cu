@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     const uint32_t idO = umma_idesc_bf16(C::M, 64 * C::CPS, true);   // the V blocks of a slot, LBO = CHUNK
     bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0) && mbar_wait(qt_full, 0));
     tc_fence_after();
+    const uint64_t qd0 = umma_desc_sw128(smem_u32(qs), 16, 1024);   // Q's shared-memory blocks
     int e = 0;
     auto take = [&]() -> uint32_t {   // wait for the next ring slot, return its address
       const int sl = e % C::NSLOT;
@@ -390,22 +391,23 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         for (int kp = 0; ok && kp < C::KB; kp += C::CPS) {
           const uint32_t sbase = take();   // K chunks kp .. kp + CPS - 1
           if (!ok) break;
+          // one descriptor per slot; within it an operand at byte offset off
+          // has descriptor d0 + off / 16 (start-address field, no carry: every
+          // shared-memory address is below 256 KB)
+          const uint64_t kd0 = umma_desc_sw128(sbase, 16, 1024);
           if (elect_one()) {
 #pragma unroll
             for (int h = 0; h < C::CPS; ++h) {
               const int kb = kp + h;
-              const uint32_t kbase = sbase + h * C::CHUNK;
+              const uint64_t kd = kd0 + static_cast<uint64_t>(h * C::CHUNK / 16);
               if (kb < C::NQT) {   // A = Q block from tensor memory
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                  umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, umma_desc_sw128(kbase + ks * 32, 16, 1024),
-                          idS, (kb > 0 || ks > 0) ? 1u : 0u);
+                  umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, kd + 2 * ks, idS, (kb > 0 || ks > 0) ? 1u : 0u);
               } else {             // A = Q block from shared memory
-                const uint32_t qb = smem_u32(qs + (kb - C::NQT) * (C::M * 128));
+                const uint64_t qd = qd0 + static_cast<uint64_t>((kb - C::NQT) * (C::M * 128) / 16);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                  umma_ss(s_tmem, umma_desc_sw128(qb + ks * 32, 16, 1024), umma_desc_sw128(kbase + ks * 32, 16, 1024),
-                          idS, 1u);
+                for (int ks = 0; ks < 4; ++ks) umma_ss(s_tmem, qd + 2 * ks, kd + 2 * ks, idS, 1u);
               }
             }
           }
@@ -424,11 +426,12 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         for (int i4 = 0; ok && i4 < C::NVB; i4 += C::CPS) {
           const uint32_t vbase = take();   // V blocks i4 ..: 64 keys x 64 CPS output columns, MN-major
           if (!ok) break;
+          const uint64_t vd0 = umma_desc_sw128(vbase, C::CHUNK, 1024);
           if (elect_one()) {
 #pragma unroll
             for (int ks = 0; ks < C::NK / 16; ++ks)
-              umma_ts(tmem + i4 * 64, tmem + C::S_COL0 + sb * 64 + ks * 8,
-                      umma_desc_sw128(vbase + ks * 2048, C::CHUNK, 1024), idO, (i > 0 || ks > 0) ? 1u : 0u);
+              umma_ts(tmem + i4 * 64, tmem + C::S_COL0 + sb * 64 + ks * 8, vd0 + static_cast<uint64_t>(ks * 2048 / 16),
+                      idO, (i > 0 || ks > 0) ? 1u : 0u);
           }
           __syncwarp();
           give();
