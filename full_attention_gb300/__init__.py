@@ -23,6 +23,7 @@ DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE = 
 FLAG_EARLY_METADATA = 1
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
+MAX_LAYERS_PER_LAUNCH = 16
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_NOT_BOUND, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4, 5
 
@@ -57,6 +58,9 @@ def _load() -> ctypes.CDLL:
         "fa_paged_decode_attn": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_store_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_attn_noalloc": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
+        "fa_kv_store_layers": (i32, [vp, i32, vp, vp, vp, vp, i32, vp]),
+        "fa_decode_layers_workspace_bytes": (sz, [vp, i32, vp, i32, i32]),
+        "fa_paged_decode_attn_layers": (i32, [vp, i32, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "fa_get_device_error": (i32, [ctypes.POINTER(i32), vp]),
         "fa_last_error": (ctypes.c_char_p, []),
@@ -90,6 +94,15 @@ def _s(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptrs(ts):
+    """A host array of device pointers (NULL for None), kept alive by the caller."""
+    return (ctypes.c_void_p * len(ts))(*[None if t is None else t.data_ptr() for t in ts])
+
+
+def _i32s(xs):
+    return (ctypes.c_int32 * len(xs))(*[int(x) for x in xs])
 
 
 def _desc(d: dict) -> LayerDesc:
@@ -168,6 +181,26 @@ class Cache:
     def store(self, layer: int, k, v, slot_mapping, stream=None) -> None:
         _check(_lib.fa_kv_store(self._h, layer, _p(k), _p(v), _p(slot_mapping), int(slot_mapping.numel()),
                                 _s(stream)))
+
+    def store_layers(self, layers, ks, vs, slot_mappings, stream=None) -> None:
+        """fa_kv_store_layers: the stores of several layers in one launch
+        (shared layers are skipped)."""
+        T = int(slot_mappings[0].numel())
+        _check(_lib.fa_kv_store_layers(self._h, len(layers), _i32s(layers), _ptrs(ks), _ptrs(vs),
+                                       _ptrs(slot_mappings), T, _s(stream)))
+
+    def decode_layers_workspace_bytes(self, layers, batch: int, max_seq_len: int) -> int:
+        return int(_lib.fa_decode_layers_workspace_bytes(self._h, len(layers), _i32s(layers), batch, max_seq_len))
+
+    def decode_layers(self, layers, qs, block_tables, seq_lens, max_seq_len: int, outs, lses=None,
+                      workspace=None, stream=None) -> None:
+        """fa_paged_decode_attn_layers: decode several layers of one head_dim
+        in one launch (the current rows must already be stored)."""
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(_lib.fa_paged_decode_attn_layers(self._h, len(layers), _i32s(layers), _ptrs(qs), _ptrs(block_tables),
+                                                int(block_tables[0].shape[1]), _p(seq_lens), int(qs[0].shape[0]),
+                                                int(max_seq_len), _ptrs(outs), None if lses is None else _ptrs(lses),
+                                                _p(workspace), ws_bytes, _s(stream)))
 
     def decode_workspace_bytes(self, layer: int, batch: int, max_seq_len: int) -> int:
         return int(_lib.fa_decode_workspace_bytes(self._h, layer, batch, max_seq_len))

@@ -414,36 +414,57 @@ size_t fa_decode_workspace_bytes(const fa_cache* c, int32_t layer, int32_t B, in
   return plan_decode(c, layer, B, max_seq_len).ws_bytes;
 }
 
-namespace fa {
-// Decode with an optional store of the current token (k_new, v_new, slots
-// non-null for an owning layer).
-static fa_status decode_call(fa_cache* c, int32_t layer, const void* q, const void* k_new, const void* v_new,
-                             const int32_t* slots, const int32_t* block_table, int32_t max_pages_per_seq,
-                             const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out, float* lse,
-                             void* workspace, size_t workspace_bytes, void* stream) {
-  fa_status st = check_layer(c, layer);
-  if (st) return st;
-  if (B < 0) return fail(FA_ERR_INVALID_ARG, "B must be >= 0");
-  if (B == 0) return ok();
-  const Layer& L = c->layers[layer];
-  const Slab* s = nullptr;
-  if ((st = check_bound(c, layer, &s))) return st;
-  if (!q || !block_table || !seq_lens || !out)
-    return fail(FA_ERR_INVALID_ARG, "q, block_table, seq_lens, out must be non-NULL");
-  if (!aligned16(q) || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "q, out must be 16-byte aligned");
-  if (max_seq_len < 1) return fail(FA_ERR_INVALID_ARG, "max_seq_len must be >= 1");
-  if (max_pages_per_seq < (max_seq_len + c->page_size - 1) / c->page_size)
-    return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_seq_len %d", max_pages_per_seq,
-                max_seq_len);
-  DecodePlan p = plan_decode(c, layer, B, max_seq_len);
-  if (workspace_bytes < p.ws_bytes || (p.ws_bytes && !workspace))
-    return fail(FA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, p.ws_bytes);
-  if (p.ws_bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+fa_status fa_kv_store_layers(fa_cache* c, int32_t n, const int32_t* layers, const void* const* k,
+                             const void* const* v, const int32_t* const* slot_mapping, int32_t T, void* stream) {
+  if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
+  if (n < 1 || n > FA_MAX_LAYERS_PER_LAUNCH) return fail(FA_ERR_INVALID_ARG, "n must be in [1, %d]", FA_MAX_LAYERS_PER_LAUNCH);
+  if (!layers || !k || !v || !slot_mapping) return fail(FA_ERR_INVALID_ARG, "layers, k, v, slot_mapping must be non-NULL");
+  if (T < 0) return fail(FA_ERR_INVALID_ARG, "T must be >= 0");
+  fa_status st;
+  StoreArgs a[FA_MAX_LAYERS_PER_LAUNCH];
+  int m = 0;
   cudaError_t ce;
   unsigned int* err = device_error_word(&ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
-  DecodeArgs a{};
+  for (int i = 0; i < n; ++i) {
+    if ((st = check_layer(c, layers[i]))) return st;
+    for (int j = 0; j < i; ++j)
+      if (layers[j] == layers[i]) return fail(FA_ERR_INVALID_ARG, "layer %d listed twice", layers[i]);
+    const Layer& L = c->layers[layers[i]];
+    if (L.owner != layers[i] || T == 0) continue;   // a shared layer stores nothing
+    const Slab* s = nullptr;
+    if ((st = check_bound(c, layers[i], &s))) return st;
+    if (!k[i] || !v[i] || !slot_mapping[i]) return fail(FA_ERR_INVALID_ARG, "k, v, slot_mapping of layer %d must be non-NULL", layers[i]);
+    if (!aligned16(k[i]) || !aligned16(v[i])) return fail(FA_ERR_INVALID_ARG, "k, v of layer %d must be 16-byte aligned", layers[i]);
+    a[m++] = StoreArgs{k[i], v[i], slot_mapping[i], s->k, s->v, s->k_scale, s->v_scale, T, L.d.num_kv_heads,
+                       L.d.head_dim, c->page_size, c->num_pages, c->kv_dtype,
+                       (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0, err};
+  }
+  if (m == 0) return ok();
+  ce = launch_store_layers(a, m, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "store launch: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
+size_t fa_decode_layers_workspace_bytes(const fa_cache* c, int32_t n, const int32_t* layers, int32_t B,
+                                        int32_t max_seq_len) {
+  if (!c || !layers || n < 1 || n > FA_MAX_LAYERS_PER_LAUNCH || B <= 0 || max_seq_len <= 0) return 0;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    if (check_layer(c, layers[i]) != FA_OK) return 0;
+    total += (plan_decode(c, layers[i], B, max_seq_len).ws_bytes + 255) / 256 * 256;
+  }
+  return total;
+}
+
+namespace fa {
+// The launch arguments of one layer's decode (validated by the caller).
+static void fill_decode_args(DecodeArgs& a, const fa_cache* c, int32_t layer, const Slab* s, const DecodePlan& p,
+                             const void* q, const void* k_new, const void* v_new, const int32_t* slots,
+                             const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens,
+                             int32_t B, int32_t max_seq_len, void* out, float* lse, void* workspace,
+                             unsigned int* err) {
+  const Layer& L = c->layers[layer];
   a.q = q;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
@@ -476,10 +497,45 @@ static fa_status decode_call(fa_cache* c, int32_t layer, const void* q, const vo
   a.sm_scale = L.d.sm_scale;
   a.plan = p;
   a.err = err;
+}
+
+// Decode with an optional store of the current token (k_new, v_new, slots
+// non-null for an owning layer).
+static fa_status decode_call(fa_cache* c, int32_t layer, const void* q, const void* k_new, const void* v_new,
+                             const int32_t* slots, const int32_t* block_table, int32_t max_pages_per_seq,
+                             const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_layer(c, layer);
+  if (st) return st;
+  if (B < 0) return fail(FA_ERR_INVALID_ARG, "B must be >= 0");
+  if (B == 0) return ok();
+  const Layer& L = c->layers[layer];
+  const Slab* s = nullptr;
+  if ((st = check_bound(c, layer, &s))) return st;
+  if (!q || !block_table || !seq_lens || !out)
+    return fail(FA_ERR_INVALID_ARG, "q, block_table, seq_lens, out must be non-NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "q, out must be 16-byte aligned");
+  if (max_seq_len < 1) return fail(FA_ERR_INVALID_ARG, "max_seq_len must be >= 1");
+  if (max_pages_per_seq < (max_seq_len + c->page_size - 1) / c->page_size)
+    return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_seq_len %d", max_pages_per_seq,
+                max_seq_len);
+  DecodePlan p = plan_decode(c, layer, B, max_seq_len);
+  if (workspace_bytes < p.ws_bytes || (p.ws_bytes && !workspace))
+    return fail(FA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, p.ws_bytes);
+  if (p.ws_bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  cudaError_t ce;
+  unsigned int* err = device_error_word(&ce);
+  if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
+  (void)L;
+  DecodeArgs a{};
+  fill_decode_args(a, c, layer, s, p, q, k_new, v_new, slots, block_table, max_pages_per_seq, seq_lens, B,
+                   max_seq_len, out, lse, workspace, err);
   ce = launch_decode(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
   return ok();
 }
+
 }  // namespace fa
 
 fa_status fa_paged_decode_attn(fa_cache* c, int32_t layer, const void* q, const int32_t* block_table,
@@ -507,6 +563,56 @@ fa_status fa_paged_decode_store_attn(fa_cache* c, int32_t layer, const void* q, 
   }
   return decode_call(c, layer, q, k_new, v_new, slot_mapping, block_table, max_pages_per_seq, seq_lens, B,
                      max_seq_len, out, lse, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_paged_decode_attn_layers(fa_cache* c, int32_t n, const int32_t* layers, const void* const* q,
+                                      const int32_t* const* block_table, int32_t max_pages_per_seq,
+                                      const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* const* out,
+                                      float* const* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
+  if (n < 1 || n > FA_MAX_LAYERS_PER_LAUNCH) return fail(FA_ERR_INVALID_ARG, "n must be in [1, %d]", FA_MAX_LAYERS_PER_LAUNCH);
+  if (!layers || !q || !block_table || !out) return fail(FA_ERR_INVALID_ARG, "layers, q, block_table, out must be non-NULL");
+  if (B < 0) return fail(FA_ERR_INVALID_ARG, "B must be >= 0");
+  if (!seq_lens) return fail(FA_ERR_INVALID_ARG, "seq_lens must be non-NULL");
+  if (max_seq_len < 1) return fail(FA_ERR_INVALID_ARG, "max_seq_len must be >= 1");
+  if (max_pages_per_seq < (max_seq_len + c->page_size - 1) / c->page_size)
+    return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_seq_len %d", max_pages_per_seq, max_seq_len);
+  fa_status st;
+  int D = 0;
+  for (int i = 0; i < n; ++i) {
+    if ((st = check_layer(c, layers[i]))) return st;
+    for (int j = 0; j < i; ++j)
+      if (layers[j] == layers[i]) return fail(FA_ERR_INVALID_ARG, "layer %d listed twice", layers[i]);
+    const int d = c->layers[layers[i]].d.head_dim;
+    if (i == 0) D = d;
+    else if (d != D) return fail(FA_ERR_UNSUPPORTED, "layers of head_dim %d and %d in one call", D, d);
+    if (!q[i] || !block_table[i] || !out[i]) return fail(FA_ERR_INVALID_ARG, "q, block_table, out of layer %d must be non-NULL", layers[i]);
+    if (!aligned16(q[i]) || !aligned16(out[i])) return fail(FA_ERR_INVALID_ARG, "q, out of layer %d must be 16-byte aligned", layers[i]);
+  }
+  if (B == 0) return ok();
+  const size_t need = fa_decode_layers_workspace_bytes(c, n, layers, B, max_seq_len);
+  if (workspace_bytes < need || (need && !workspace))
+    return fail(FA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (need && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  cudaError_t ce;
+  unsigned int* err = device_error_word(&ce);
+  if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
+  DecodeArgs a[FA_MAX_LAYERS_PER_LAUNCH];
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    const Slab* s = nullptr;
+    if ((st = check_bound(c, layers[i], &s))) return st;
+    const DecodePlan p = plan_decode(c, layers[i], B, max_seq_len);
+    a[i] = DecodeArgs{};
+    fill_decode_args(a[i], c, layers[i], s, p, q[i], nullptr, nullptr, nullptr, block_table[i], max_pages_per_seq,
+                     seq_lens, B, max_seq_len, out[i], lse ? lse[i] : nullptr,
+                     p.ws_bytes ? static_cast<char*>(workspace) + off : nullptr, err);
+    off += (p.ws_bytes + 255) / 256 * 256;
+  }
+  ce = launch_decode_layers(a, n, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
+  return ok();
 }
 
 fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const void* k_ext, const void* v_ext,

@@ -366,11 +366,12 @@ __device__ void merge_unit(const DecK& p, int u, const Unit& x, int nh, int head
   named_bar_sync(1, 128);   // the scratch (the score-exchange buffer) is free again
 }
 
+// One CTA of a layer's decode: CTA `cta` of the `grid` CTAs launched for the
+// layer (a launch may hold several layers; see decode_layers_kernel).
 template <int D, int KV>
-__global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
-                  const DecK p) {
+__device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, const DecK& p,
+                                            const int cta, const int grid) {
   using C = DecCfg<D, KV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
       Unit x{};
       if (u < p.units) {
         x = unit_of(p, u);
-        if (blockIdx.x == 0 && __ldg(p.seq_lens + x.b) > p.max_seq_len) atomicOr(p.err, FA_DEV_ERR_BOUND);
+        if (cta == 0 && __ldg(p.seq_lens + x.b) > p.max_seq_len) atomicOr(p.err, FA_DEV_ERR_BOUND);
       }
       int tot;
       const int P = running + block_excl_scan(x.n, sm_scan, &tot);
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
     }
     T = running;
   }
-  int ncta = (T == 0) ? 0 : min(static_cast<int>(gridDim.x), max(1, (T + p.min_tiles - 1) / p.min_tiles));
+  int ncta = (T == 0) ? 0 : min(grid, max(1, (T + p.min_tiles - 1) / p.min_tiles));
   int kper = 0;   // CTAs per unit of the unit-aligned cut (0: concatenated cut)
   if (ncta > 0 && p.units <= static_cast<int>(blockDim.x)) {
     const bool mine = static_cast<int>(threadIdx.x) < p.units;
@@ -438,17 +439,17 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
       }
     }
   }
-  if (static_cast<int>(blockIdx.x) >= ncta) {
-    if (ncta == 0 && blockIdx.x == 0) {   // nothing visible anywhere: only empty outputs to write
+  if (cta >= ncta) {
+    if (ncta == 0 && cta == 0) {   // nothing visible anywhere: only empty outputs to write
       griddep_wait();
       zero_empty_units<D, KV>(p, 0, 1, threadIdx.x, blockDim.x);
     }
     return;
   }
-  long long s_beg = static_cast<long long>(blockIdx.x) * T / ncta;
-  long long s_end = static_cast<long long>(blockIdx.x + 1) * T / ncta;
+  long long s_beg = static_cast<long long>(cta) * T / ncta;
+  long long s_end = static_cast<long long>(cta + 1) * T / ncta;
   if (kper) {
-    if (static_cast<int>(threadIdx.x) == static_cast<int>(blockIdx.x) / kper) {
+    if (static_cast<int>(threadIdx.x) == cta / kper) {
       sh_u0 = threadIdx.x;
       sh_p0 = my_P;
       sh_n0 = my_n;
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   __syncthreads();
   const int u0 = sh_u0, p0 = sh_p0;
   if (kper) {   // part r of unit u0
-    const int r = static_cast<int>(blockIdx.x) % kper, n0 = sh_n0;
+    const int r = cta % kper, n0 = sh_n0;
     s_beg = p0 + static_cast<long long>(r) * n0 / kper;
     s_end = p0 + static_cast<long long>(r + 1) * n0 / kper;
   }
@@ -494,8 +495,8 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
   if (warp == C::NCW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+      prefetch_tmap(tm_k);
+      prefetch_tmap(tm_v);
     }
     const uint64_t pol = l2_policy_evict_first();
     int gi = 0, j = 0;
@@ -578,12 +579,12 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
                   const int tile = k + t;
                   const int row0 = (pg[t] * p.Hkv + x.h) * p.page_size + (tile % p.tiles_per_page) * kTile;
                   // one copy per tile: all column blocks of 16 rows
-                  tma_load_3d(kdst + t * C::TILE_BYTES, &tm_k, &full[st], 0, row0, 0, pol);
-                  tma_load_3d(vdst + t * C::TILE_BYTES, &tm_v, &full[st], 0, row0, 0, pol);
+                  tma_load_3d(kdst + t * C::TILE_BYTES, tm_k, &full[st], 0, row0, 0, pol);
+                  tma_load_3d(vdst + t * C::TILE_BYTES, tm_v, &full[st], 0, row0, 0, pol);
                   if constexpr (KV) {
                     float* sc = reinterpret_cast<float*>(smem + C::OFF_SC + st * C::SC_BYTES);
-                    tma_load_2d(sc + t * 32, &tm_ks, &full[st], 0, row0 / kTile, pol);
-                    tma_load_2d(sc + (C::NT + t) * 32, &tm_vs, &full[st], 0, row0 / kTile, pol);
+                    tma_load_2d(sc + t * 32, tm_ks, &full[st], 0, row0 / kTile, pol);
+                    tma_load_2d(sc + (C::NT + t) * 32, tm_vs, &full[st], 0, row0 / kTile, pol);
                   }
                 }
               }
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
 
   // -------------------------------------------------------------- consumers
   griddep_wait();
-  zero_empty_units<D, KV>(p, blockIdx.x, ncta, threadIdx.x, C::NCW * 32);
+  zero_empty_units<D, KV>(p, cta, ncta, threadIdx.x, C::NCW * 32);
   const int qk_tile = warp % C::NT;
   const int qk_d0 = (warp / C::NT) * C::QK_COLS;
   const int pv_d0 = warp * C::PV_COLS;
@@ -883,7 +884,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
         if (p.lse && warp == 0 && tig == 0 && hv)
           p.lse[static_cast<size_t>(x.b) * p.Hq + head0 + gid] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       } else {
-        const size_t slot = static_cast<size_t>(blockIdx.x) + u;
+        const size_t slot = static_cast<size_t>(cta) + u;
 #pragma unroll
         for (int mt = 0; mt < C::PV_MT; ++mt)
 #pragma unroll
@@ -927,6 +928,33 @@ consumers_done:;
 }
 
 template <int D, int KV>
+__global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
+                  const DecK p) {
+  decode_body<D, KV>(&tm_k, &tm_v, &tm_ks, &tm_vs, p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
+}
+
+// Several layers of one head_dim and KV format in one launch: the CTAs of
+// layer i are [cta0[i], cta0[i + 1]); each runs exactly as in a launch of
+// its own, with its own parameters, tensor maps and workspace region.
+struct DecLayers {
+  CUtensorMap tm[kMaxLayersPerLaunch][4];   // K, V, K scale, V scale
+  DecK k[kMaxLayersPerLaunch];
+  int cta0[kMaxLayersPerLaunch + 1];
+  int n;
+};
+
+template <int D, int KV>
+__global__ void __launch_bounds__(DecCfg<D, KV>::NTHR, 2) decode_layers_kernel(const __grid_constant__ DecLayers m) {
+  const int b = static_cast<int>(blockIdx.x);
+  int li = 0;
+  while (li + 1 < m.n && b >= m.cta0[li + 1]) ++li;
+  decode_body<D, KV>(&m.tm[li][0], &m.tm[li][1], &m.tm[li][2], &m.tm[li][3], m.k[li], b - m.cta0[li],
+                     m.cta0[li + 1] - m.cta0[li]);
+}
+
+template <int D, int KV>
 static cudaError_t launch_decode_t(const DecodeArgs& a, const DecK& k, cudaStream_t s) {
   using C = DecCfg<D, KV>;
   static unsigned int done = 0;
@@ -937,7 +965,17 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const DecK& k, cudaStrea
   return e;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+template <int D, int KV>
+static cudaError_t launch_decode_layers_t(const DecLayers& m, cudaStream_t s) {
+  using C = DecCfg<D, KV>;
+  static unsigned int done = 0;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_layers_kernel<D, KV>), C::SMEM_ALLOC, &done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_layers_kernel<D, KV>, dim3(m.cta0[m.n]), dim3(C::NTHR), C::SMEM_ALLOC, s, m);
+}
+
+// The kernel parameters of one layer's decode.
+static DecK make_deck(const DecodeArgs& a) {
   DecK k{};
   k.q = static_cast<const __nv_bfloat16*>(a.q);
   k.block_table = a.block_table;
@@ -974,12 +1012,38 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   k.min_tiles = a.plan.min_tiles;
   k.early_metadata = a.early_metadata;
   k.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  return k;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const DecK k = make_deck(a);
   if (a.kv_dtype == FA_KV_INT8) {
     if (a.D == 256) return launch_decode_t<256, 1>(a, k, s);
     return launch_decode_t<512, 1>(a, k, s);
   }
   if (a.D == 256) return launch_decode_t<256, 0>(a, k, s);
   return launch_decode_t<512, 0>(a, k, s);
+}
+
+cudaError_t launch_decode_layers(const DecodeArgs* a, int n, cudaStream_t s) {
+  if (n < 1 || n > kMaxLayersPerLaunch) return cudaErrorInvalidValue;
+  DecLayers m{};   // the kernel parameters (copied at launch)
+  m.n = n;
+  m.cta0[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    m.tm[i][0] = *a[i].tm_k;
+    m.tm[i][1] = *a[i].tm_v;
+    m.tm[i][2] = *a[i].tm_ks;
+    m.tm[i][3] = *a[i].tm_vs;
+    m.k[i] = make_deck(a[i]);
+    m.cta0[i + 1] = m.cta0[i] + a[i].plan.ncta;
+  }
+  if (a[0].kv_dtype == FA_KV_INT8) {
+    if (a[0].D == 256) return launch_decode_layers_t<256, 1>(m, s);
+    return launch_decode_layers_t<512, 1>(m, s);
+  }
+  if (a[0].D == 256) return launch_decode_layers_t<256, 0>(m, s);
+  return launch_decode_layers_t<512, 0>(m, s);
 }
 
 // ---------------------------------------------------------------------------

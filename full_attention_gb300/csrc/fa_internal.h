@@ -14,6 +14,8 @@ namespace fa {
 // Token rows are processed in 16-row tiles: one m16 tile of the warp MMAs and
 // one TMA box height.  Page sizes are multiples of it.
 constexpr int kTile = 16;
+// Layers one multi-layer launch can hold.
+constexpr int kMaxLayersPerLaunch = FA_MAX_LAYERS_PER_LAUNCH;
 
 struct Slab {
   void* k = nullptr;
@@ -111,6 +113,8 @@ struct StoreArgs {
   unsigned int* err;
 };
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s);
+// The stores of several layers in one launch (n <= kMaxLayersPerLaunch; any head_dim mix).
+cudaError_t launch_store_layers(const StoreArgs* a, int n, cudaStream_t s);
 
 struct DecodeArgs {
   const void* q;
@@ -137,6 +141,8 @@ struct DecodeArgs {
   unsigned int* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// Several layers of one head_dim and KV format in one launch (n <= kMaxLayersPerLaunch).
+cudaError_t launch_decode_layers(const DecodeArgs* a, int n, cudaStream_t s);
 
 struct ExtendArgs {
   const void* q;

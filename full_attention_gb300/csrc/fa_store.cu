@@ -6,6 +6,7 @@
 // and stores.  The int8 per-token-head format quantises the row on the way:
 // a = max|x| (fp32, warp-shuffle reduction), s = a / 127, c = rint(x / s)
 // clamped to [-127, 127], both divisions IEEE round-to-nearest.
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -41,12 +42,10 @@ unsigned int* device_error_word(cudaError_t* err) {
   return ptrs[dev];
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
-  if (!a.early_metadata) griddep_wait();
-  griddep_launch_dependents();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+// One (token, KV head, K or V) row per warp; `warp` counts the launch's
+// warps for this layer.
+template <int D, int KV>
+__device__ __forceinline__ void store_row(const StoreArgs& a, int warp, int lane) {
   const int rows = a.T * a.Hkv * 2;
   if (warp >= rows) return;
   const int which = warp & 1;            // 0: K, 1: V
@@ -62,34 +61,58 @@ __global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
   griddep_wait();   // the rows (and the slab) may belong to the previous kernel
   RowRegs<D> r;
   row_load<D>(r, static_cast<const __nv_bfloat16*>(which ? a.v : a.k) + (static_cast<size_t>(t) * a.Hkv + h) * D, lane);
-  row_store_bf16<D>(r, static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) +
-                           ((static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off) * D, lane);
+  const size_t row = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
+  if constexpr (KV) {
+    row_store_int8<D>(r, static_cast<int8_t*>(which ? a.v_slab : a.k_slab) + row * D,
+                      (which ? a.v_scale : a.k_scale) + row, lane);
+  } else {
+    row_store_bf16<D>(r, static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) + row * D, lane);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
+  if (!a.early_metadata) griddep_wait();
+  griddep_launch_dependents();
+  store_row<D, 0>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
 }
 
 template <int D>
 __global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
   if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int rows = a.T * a.Hkv * 2;
-  if (warp >= rows) return;
-  const int which = warp & 1;
-  const int th = warp >> 1;
-  const int t = th / a.Hkv, h = th % a.Hkv;
-  const int slot = __ldg(a.slots + t);
-  if (slot < 0) return;
-  const int page = slot / a.page_size, off = slot % a.page_size;
-  if (page >= a.num_pages) {
-    if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
-    return;
+  store_row<D, 1>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
+}
+
+// Several layers' stores in one launch: blockIdx.y picks the layer.
+struct StoreLayers {
+  StoreArgs a[kMaxLayersPerLaunch];
+};
+
+template <int KV>
+__global__ void __launch_bounds__(256) store_layers_kernel(const __grid_constant__ StoreLayers m) {
+  const StoreArgs& a = m.a[blockIdx.y];
+  if (!a.early_metadata) griddep_wait();
+  griddep_launch_dependents();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (a.D == 256) store_row<256, KV>(a, warp, lane);
+  else store_row<512, KV>(a, warp, lane);
+}
+
+cudaError_t launch_store_layers(const StoreArgs* a, int n, cudaStream_t s) {
+  if (n < 1 || n > kMaxLayersPerLaunch) return cudaErrorInvalidValue;
+  StoreLayers m{};
+  long warps = 0;
+  for (int i = 0; i < n; ++i) {
+    m.a[i] = a[i];
+    warps = std::max(warps, static_cast<long>(a[i].T) * a[i].Hkv * 2);
   }
-  griddep_wait();   // the rows (and the slab) may belong to the previous kernel
-  RowRegs<D> r;
-  row_load<D>(r, static_cast<const __nv_bfloat16*>(which ? a.v : a.k) + (static_cast<size_t>(t) * a.Hkv + h) * D, lane);
-  const size_t row = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
-  row_store_int8<D>(r, static_cast<int8_t*>(which ? a.v_slab : a.k_slab) + row * D,
-                    (which ? a.v_scale : a.k_scale) + row, lane);
+  const int block = 256;
+  const long grid = (warps * 32 + block - 1) / block;
+  if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
+  const dim3 g(static_cast<unsigned>(grid), static_cast<unsigned>(n)), b(block);
+  if (a[0].kv_dtype == FA_KV_INT8) return launch_pdl(store_layers_kernel<1>, g, b, 0, s, m);
+  return launch_pdl(store_layers_kernel<0>, g, b, 0, s, m);
 }
 
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {

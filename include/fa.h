@@ -243,6 +243,47 @@ FA_API fa_status fa_paged_decode_store_attn(fa_cache* cache, int32_t layer, cons
                                      int32_t max_seq_len, void* out, float* lse, void* workspace,
                                      size_t workspace_bytes, void* stream);
 
+/* Most layers one multi-layer store or decode call takes. */
+#define FA_MAX_LAYERS_PER_LAUNCH 16
+
+/* The stores of n layers in one launch: the effect of fa_kv_store(cache,
+ * layers[i], k[i], v[i], slot_mapping[i], T) for i = 0 .. n - 1 (host arrays
+ * of n device pointers; shared layers are skipped, layers of both head_dims
+ * may be mixed).  1 <= n <= FA_MAX_LAYERS_PER_LAUNCH; the layers must be
+ * distinct owning or shared layers of the cache.  Every row of every layer
+ * is stored before the call's stream moves on, so decode calls that follow
+ * see all of them. */
+FA_API fa_status fa_kv_store_layers(fa_cache* cache, int32_t n, const int32_t* layers, const void* const* k,
+                                    const void* const* v, const int32_t* const* slot_mapping, int32_t T,
+                                    void* stream);
+
+/* Workspace bytes fa_paged_decode_attn_layers needs: the per-layer
+ * workspaces of the n layers laid end to end (each 256-byte aligned).  0 on
+ * invalid arguments.  Host only. */
+FA_API size_t fa_decode_layers_workspace_bytes(const fa_cache* cache, int32_t n, const int32_t* layers,
+                                               int32_t B, int32_t max_seq_len);
+
+/* Paged decode attention of n layers in one launch: the same result per
+ * layer, bit for bit, as fa_paged_decode_attn on that layer, with one launch
+ * ramp and one tail for all of them instead of one each.  For callers that have the queries of
+ * several layers at once: a step that decodes several independent layer
+ * stacks, or a benchmark of the attention of a whole step.  The layers must
+ * share head_dim and the cache's KV format (a full and a sliding group take
+ * two calls) and be distinct; shared layers read their source's slab, so
+ * the current token's rows must already be stored (fa_kv_store or
+ * fa_kv_store_layers; there is no fused store here).  q, block_table, out,
+ * lse: host arrays of n device pointers, per layer as in
+ * fa_paged_decode_attn (lse[i] may be NULL; lse itself may be NULL for no
+ * lse at all).  seq_lens, B, max_seq_len and max_pages_per_seq are common to
+ * all layers.  workspace: at least fa_decode_layers_workspace_bytes bytes,
+ * 256-byte aligned, zeroed once, left zero by every completed call (as for
+ * fa_paged_decode_attn).  1 <= n <= FA_MAX_LAYERS_PER_LAUNCH. */
+FA_API fa_status fa_paged_decode_attn_layers(fa_cache* cache, int32_t n, const int32_t* layers,
+                                             const void* const* q, const int32_t* const* block_table,
+                                             int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t B,
+                                             int32_t max_seq_len, void* const* out, float* const* lse,
+                                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Largest scratch the allocation-free decode below can use (bytes). */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 
