@@ -213,9 +213,21 @@ class DecodeStep:
             sl = torch.from_numpy(W.decode_slot_mapping(self.lens, self.tables[i], w.page_size)).to(device)
             self.new[i] = (W.randn_bf16((self.B, d["num_kv_heads"], d["head_dim"]), s0 + 200 + i, device),
                            W.randn_bf16((self.B, d["num_kv_heads"], d["head_dim"]), s0 + 300 + i, device), sl)
+        # the multi-layer variant of the step: one store launch for the owning
+        # layers, then one decode launch per head_dim group
+        self.groups = [g for g in ([i for i, d in enumerate(self.layers) if d["head_dim"] == D] for D in (256, 512)) if g]
+        self.ws_group = []
+        for g in self.groups:
+            n = self.cache.decode_layers_workspace_bytes(g, self.B, self.max_len)
+            self.ws_group.append(fa.workspace(n, device) if n else None)
         self.decode_bytes = [decode_bytes(d, self.lens, w.kv_dtype) for d in self.layers]
         self.store_bytes = sum(store_bytes(self.layers[i], self.B, w.kv_dtype) for i in self.slabs)
         self.step_bytes = sum(self.decode_bytes) + self.store_bytes
+        # the same step with each slab's K/V counted once (a KV-shared layer
+        # reads its source's pages again; what DRAM must serve at least)
+        qo = [self.B * d["num_q_heads"] * (2 * d["head_dim"] * 2 + 4) for d in self.layers]
+        self.unique_bytes = sum(self.decode_bytes[i] for i in self.slabs) + \
+            sum(qo[i] for i in range(len(self.layers)) if self.src[i] != i) + self.store_bytes
         torch.cuda.synchronize()
 
     def _fill_int8(self, i, s0):
@@ -234,6 +246,16 @@ class DecodeStep:
 
     def launches_per_step(self):
         return len(self.layers)   # one launch per layer: owning layers store their rows in it
+
+    def run_layers(self):
+        """The same step through the multi-layer calls: the owning layers'
+        stores in one launch, then one decode launch per head_dim group."""
+        own = sorted(self.slabs)
+        self.cache.store_layers(own, [self.new[i][0] for i in own], [self.new[i][1] for i in own],
+                                [self.new[i][2] for i in own])
+        for g, ws in zip(self.groups, self.ws_group):
+            self.cache.decode_layers(g, [self.q[i] for i in g], [self.bt[i] for i in g], self.lens_dev,
+                                     self.max_len, [self.out[i] for i in g], [self.lse[i] for i in g], ws)
 
     def run(self, events=None):
         for i in range(len(self.layers)):
@@ -359,6 +381,8 @@ def gpu_arm(args, rank, world):
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(step.B * world / t_max, 1),
         "pct_of_peak": round(100 * step.step_bytes / t_max / 1e9 / hbm, 1),
+        "unique_bytes_per_step": int(step.unique_bytes),
+        "unique_gb_per_s": round(step.unique_bytes * world / t_max / 1e9, 1),
         "roofline": {"kernel": "decode_kernel (paged decode attention, split-K merged in-kernel)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_source": peak_src,
@@ -370,6 +394,7 @@ def gpu_arm(args, rank, world):
         "clocks": clocks,
         "wall_s_timed": round(wall, 3),
     }
+    res["multi_layer_step"] = multi_layer_measure(step, args, torch, flush, hbm)
     if rank == 0:
         res["e2e"] = e2e_decode(step, args, torch)
         if args.workload == "e2b_decode" and not args.no_prefill:
@@ -377,6 +402,59 @@ def gpu_arm(args, rank, world):
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
         print(json.dumps(res), flush=True)
+
+
+def multi_layer_measure(step, args, torch, flush, hbm):
+    """The step through fa_kv_store_layers + fa_paged_decode_attn_layers (one
+    store launch, one decode launch per head_dim group): same bytes, same
+    outputs, fewer launch ramps and tails.  A separate figure: in a model each
+    layer's queries come from the previous layer, so the per-layer step is the
+    headline."""
+    import full_attention_gb300 as fa
+    for _ in range(3):
+        step.run_layers()
+    torch.cuda.synchronize()
+    g = None
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step.run_layers()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step.run_layers()
+        torch.cuda.synchronize()
+    except Exception as e:
+        print(f"# multi-layer graph capture failed ({e})", file=sys.stderr)
+        torch.cuda.synchronize()
+        g = None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(args.steps, 400))
+    tot = 0.0
+    for _ in range(n):
+        flush.zero_()
+        e0.record()
+        if g is not None:
+            g.replay()
+        else:
+            step.run_layers()
+        e1.record()
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    t = tot / n / 1e3
+    gbs = step.step_bytes / t / 1e9
+    ub = step.unique_bytes / t / 1e9
+    # the shared layers read their source's slab in the same launch, so those
+    # repeated reads come from L2: the step's algorithmic bytes per second can
+    # exceed the HBM peak; the roofline of this launch is the unique bytes
+    return {"value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(t * 1e3, 4),
+            "tokens_per_s": round(step.B / t, 1),
+            "unique_bytes_per_step": int(step.unique_bytes), "unique_gb_per_s": round(ub, 1),
+            "frac_unique_of_peak": round(ub / hbm, 3),
+            "launches_per_step": 1 + len(step.groups), "graph": g is not None}
 
 
 def e2e_decode(step, args, torch):

@@ -47,7 +47,7 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 static size_t elem_bytes(int kv_dtype) { return kv_dtype == FA_KV_INT8 ? 1 : 2; }
 
 // ----------------------------------------------------------------- planning
-DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len) {
+DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len, long long max_cta) {
   DecodePlan p;
   const fa_layer_desc& d = c->layers[layer].d;
   const int g = d.num_q_heads / d.num_kv_heads;
@@ -64,7 +64,7 @@ DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len) {
   const int tile_bytes = 2 * kTile * d.head_dim * static_cast<int>(elem_bytes(c->kv_dtype));
   p.min_tiles = 4 * (32768 / tile_bytes);
   const long long t_bound = static_cast<long long>(p.units) * tiles;
-  const long long slots = 2LL * sm_count();   // two resident CTAs per SM
+  const long long slots = max_cta > 0 ? max_cta : 2LL * sm_count();   // two resident CTAs per SM
   long long n = (t_bound + p.min_tiles - 1) / p.min_tiles;
   if (n > slots) n = slots;
   if (n < 1) n = 1;
@@ -446,14 +446,37 @@ fa_status fa_kv_store_layers(fa_cache* c, int32_t n, const int32_t* layers, cons
   return ok();
 }
 
+namespace fa {
+// Plans of the layers of one multi-layer decode launch.  The launch's CTAs
+// (two per SM, one wave) are shared among the layers in proportion to their
+// tile bounds: with the other layers' CTAs beside them, each layer gets
+// fewer and longer CTAs (fewer split merges) than it would launched alone.
+static void plan_decode_layers(const fa_cache* c, int n, const int32_t* layers, int B, int max_seq_len,
+                               DecodePlan* p) {
+  long long tb[FA_MAX_LAYERS_PER_LAUNCH], tot = 0;
+  for (int i = 0; i < n; ++i) {
+    p[i] = plan_decode(c, layers[i], B, max_seq_len);
+    tb[i] = static_cast<long long>(p[i].units) * p[i].max_tiles;
+    tot += tb[i];
+  }
+  const long long slots = 2LL * sm_count();
+  for (int i = 0; i < n; ++i) {
+    long long share = tot > 0 ? slots * tb[i] / tot : 1;
+    if (share < 1) share = 1;
+    if (share < p[i].ncta) p[i] = plan_decode(c, layers[i], B, max_seq_len, share);
+  }
+}
+}  // namespace fa
+
 size_t fa_decode_layers_workspace_bytes(const fa_cache* c, int32_t n, const int32_t* layers, int32_t B,
                                         int32_t max_seq_len) {
   if (!c || !layers || n < 1 || n > FA_MAX_LAYERS_PER_LAUNCH || B <= 0 || max_seq_len <= 0) return 0;
-  size_t total = 0;
-  for (int i = 0; i < n; ++i) {
+  for (int i = 0; i < n; ++i)
     if (check_layer(c, layers[i]) != FA_OK) return 0;
-    total += (plan_decode(c, layers[i], B, max_seq_len).ws_bytes + 255) / 256 * 256;
-  }
+  DecodePlan p[FA_MAX_LAYERS_PER_LAUNCH];
+  plan_decode_layers(c, n, layers, B, max_seq_len, p);
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += (p[i].ws_bytes + 255) / 256 * 256;
   return total;
 }
 
@@ -599,11 +622,13 @@ fa_status fa_paged_decode_attn_layers(fa_cache* c, int32_t n, const int32_t* lay
   unsigned int* err = device_error_word(&ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   DecodeArgs a[FA_MAX_LAYERS_PER_LAUNCH];
+  DecodePlan plans[FA_MAX_LAYERS_PER_LAUNCH];
+  plan_decode_layers(c, n, layers, B, max_seq_len, plans);
   size_t off = 0;
   for (int i = 0; i < n; ++i) {
     const Slab* s = nullptr;
     if ((st = check_bound(c, layers[i], &s))) return st;
-    const DecodePlan p = plan_decode(c, layers[i], B, max_seq_len);
+    const DecodePlan& p = plans[i];
     a[i] = DecodeArgs{};
     fill_decode_args(a[i], c, layers[i], s, p, q[i], nullptr, nullptr, nullptr, block_table[i], max_pages_per_seq,
                      seq_lens, B, max_seq_len, out[i], lse ? lse[i] : nullptr,

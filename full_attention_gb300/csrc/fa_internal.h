@@ -80,7 +80,8 @@ struct DecodePlan {
   size_t off_ml = 0, off_o = 0;   // workspace layout (bytes); counters [units] at 0
   size_t ws_bytes = 0;
 };
-DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len);
+// max_cta > 0 caps the launch's CTAs for this layer (default: two per SM).
+DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len, long long max_cta = 0);
 
 // Launch with programmatic stream serialisation (overlaps launch latency with
 // the previous kernel's tail); every kernel waits on griddepcontrol first.

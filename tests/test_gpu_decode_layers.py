@@ -114,5 +114,11 @@ def test_layers_argument_errors():
         case.cache.decode_layers([0, 1], [case.q[0], case.q[1]], [case.bt_dev[0], case.bt_dev[1]], case.lens_dev,
                                  case.max_len, [o[0], o[0].clone()], None, case.fa.workspace(16))
     assert e.value.status == fa.ERR_WORKSPACE
+    # the reported size is enough (one wave of CTAs shared by the layers: at
+    # most the per-layer workspaces end to end)
     n = case.cache.decode_layers_workspace_bytes([0, 1], 2, case.max_len)
-    assert n == sum((case.cache.decode_workspace_bytes(i, 2, case.max_len) + 255) // 256 * 256 for i in (0, 1))
+    assert 0 < n <= sum((case.cache.decode_workspace_bytes(i, 2, case.max_len) + 255) // 256 * 256 for i in (0, 1))
+    case.store_current()
+    case.cache.decode_layers([0, 1], [case.q[0], case.q[1]], [case.bt_dev[0], case.bt_dev[1]], case.lens_dev,
+                             case.max_len, [o[0], o[0].clone()], None, case.fa.workspace(n))
+    assert fa.device_error() == 0
