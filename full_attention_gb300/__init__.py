@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "fa_paged_decode_store_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_attn_noalloc": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
         "fa_kv_store_layers": (i32, [vp, i32, vp, vp, vp, vp, i32, vp]),
+        "fa_paged_decode_multi_attn": (i32, [vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
         "fa_decode_layers_workspace_bytes": (sz, [vp, i32, vp, i32, i32]),
         "fa_paged_decode_attn_layers": (i32, [vp, i32, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
@@ -229,6 +230,14 @@ class Cache:
         _check(_lib.fa_paged_decode_attn_noalloc(self._h, layer, _p(q), _p(block_table), int(block_table.shape[1]),
                                                  _p(seq_lens), int(q.shape[0]), int(max_seq_len), _p(out), _p(lse),
                                                  _s(stream)))
+
+    def decode_multi(self, layer: int, q, qo_indptr, seq_lens, block_table, max_q_len: int, max_seq_len: int, out,
+                     lse=None, stream=None) -> None:
+        """fa_paged_decode_multi_attn: several new tokens per sequence, their rows
+        already stored; every key from the slab."""
+        _check(_lib.fa_paged_decode_multi_attn(self._h, layer, _p(q), _p(qo_indptr), _p(seq_lens), _p(block_table),
+                                               int(block_table.shape[1]), int(seq_lens.numel()), int(q.shape[0]),
+                                               int(max_q_len), int(max_seq_len), _p(out), _p(lse), _s(stream)))
 
     def extend(self, layer: int, q, k_ext, v_ext, qo_indptr, prefix_lens, block_table, max_q_len: int,
                max_prefix_len: int, out, lse=None, stream=None) -> None:

@@ -707,4 +707,68 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   return ok();
 }
 
+fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, const int32_t* qo_indptr,
+                                     const int32_t* seq_lens, const int32_t* block_table, int32_t max_pages_per_seq,
+                                     int32_t B, int32_t num_tokens, int32_t max_q_len, int32_t max_seq_len, void* out,
+                                     float* lse, void* stream) {
+  fa_status st = check_layer(c, layer);
+  if (st) return st;
+  if (B < 0 || max_q_len < 0 || max_seq_len < 0 || num_tokens < 0) return fail(FA_ERR_INVALID_ARG, "negative size");
+  if (B == 0 || max_q_len == 0 || num_tokens == 0) return ok();
+  const Layer& L = c->layers[layer];
+  const int g = L.d.num_q_heads / L.d.num_kv_heads;
+  if (128 % g != 0)
+    return fail(FA_ERR_UNSUPPORTED, "multi-token decode packs Hq/Hkv = %d query heads into 128-row tiles; it must divide 128", g);
+  if (c->kv_dtype != FA_KV_BF16)
+    return fail(FA_ERR_UNSUPPORTED, "multi-token decode over the int8 per-token-head format is not built");
+  const Slab* s = nullptr;
+  if ((st = check_bound(c, layer, &s))) return st;
+  if (!q || !qo_indptr || !seq_lens || !block_table || !out) return fail(FA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(FA_ERR_INVALID_ARG, "q, out must be 16-byte aligned");
+  if (max_seq_len < 1) return fail(FA_ERR_INVALID_ARG, "max_seq_len must be >= 1");
+  if (max_pages_per_seq < (max_seq_len + c->page_size - 1) / c->page_size)
+    return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_seq_len %d", max_pages_per_seq, max_seq_len);
+  cudaError_t ce;
+  unsigned int* err = device_error_word(&ce);
+  if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
+  ExtendArgs a{};
+  a.q = q;
+  a.qo_indptr = qo_indptr;
+  a.seq_lens = seq_lens;
+  a.keys_in_pages = 1;
+  a.block_table = block_table;
+  a.k_slab = s->k;
+  a.v_slab = s->v;
+  a.k_scale = s->k_scale;
+  a.v_scale = s->v_scale;
+  a.tm_k = &s->tm_k;
+  a.tm_v = &s->tm_v;
+  a.tm_ks = &s->tm_ks;
+  a.tm_vs = &s->tm_vs;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = L.d.num_q_heads;
+  a.Hkv = L.d.num_kv_heads;
+  a.D = L.d.head_dim;
+  a.kind = L.d.kind;
+  a.window = L.d.window;
+  a.page_size = c->page_size;
+  a.num_pages = c->num_pages;
+  a.max_pages_per_seq = max_pages_per_seq;
+  a.max_q_len = max_q_len;
+  a.max_prefix_len = max_seq_len;   // bounds the sequence lengths in this mode
+  a.kv_dtype = c->kv_dtype;
+  a.num_tokens = num_tokens;
+  a.early_metadata = (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0;
+  a.sm_scale = L.d.sm_scale;
+  a.err = err;
+  if ((st = encode_q_map(&a.tm_q, q, num_tokens, L.d.num_q_heads, L.d.head_dim, g))) return st;
+  a.tm_kx = s->tm_k;   // no chunk rows in this mode: the chunk maps are never used
+  a.tm_vx = s->tm_v;
+  ce = launch_extend(a, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
+  return ok();
+}
+
 }  // extern "C"

@@ -91,12 +91,13 @@ struct ExtK {
   const uint8_t* v_ext;
   const int32_t* qo_indptr;
   const int32_t* prefix_lens;
+  const int32_t* seq_lens;   // keys_in_pages: every key (the new tokens' included) is read from the slab
   const int32_t* block_table;
   __nv_bfloat16* out;
   float* lse;
   unsigned int* err;
   int B, Hq, Hkv, g, T, kind, window, page_size, tiles_per_page, num_pages, max_pages_per_seq;
-  int max_q_len, max_prefix_len, dslices, early_metadata, num_tokens;
+  int max_q_len, max_prefix_len, dslices, early_metadata, num_tokens, keys_in_pages;
   float scale_log2;
 };
 
@@ -108,6 +109,7 @@ struct ExtK {
 // depend on the order of the tiles.
 struct ExtPlan {
   int b, h, ds, t0, n, P, qo0;
+  int Pk;                  // keys [0, Pk) come from the slab (P, or all keys when keys_in_pages)
   int kmin, kmax;          // visible key positions of the CTA's rows
   int a0, np;              // first prefix tile start, number of prefix tiles
   int c0, nc;              // first chunk tile start (absolute position), number of chunk tiles
@@ -131,11 +133,23 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   x.t0 = blockIdx.x * p.T;
   x.qo0 = __ldg(p.qo_indptr + x.b);
   x.n = __ldg(p.qo_indptr + x.b + 1) - x.qo0;
-  x.P = __ldg(p.prefix_lens + x.b);
   bool bad = false;
   if (x.n > p.max_q_len) { x.n = p.max_q_len; bad = true; }
-  if (x.P > p.max_prefix_len) { x.P = p.max_prefix_len; bad = true; }
-  if (x.P < 0 || x.n < 0) { x.P = max(x.P, 0); x.n = max(x.n, 0); bad = true; }
+  if (x.n < 0) { x.n = 0; bad = true; }
+  if (p.keys_in_pages) {
+    // the n new tokens are the sequence's last n positions, already stored;
+    // max_prefix_len bounds the sequence length
+    int L = __ldg(p.seq_lens + x.b);
+    if (L > p.max_prefix_len) { L = p.max_prefix_len; bad = true; }
+    if (L < x.n) { x.n = max(L, 0); bad = true; }
+    x.P = L - x.n;
+    x.Pk = L;
+  } else {
+    x.P = __ldg(p.prefix_lens + x.b);
+    if (x.P > p.max_prefix_len) { x.P = p.max_prefix_len; bad = true; }
+    if (x.P < 0) { x.P = 0; bad = true; }
+    x.Pk = x.P;
+  }
   if (bad && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FA_DEV_ERR_BOUND);
   if (x.t0 >= x.n) return false;
   const int q_first = x.P + x.t0;
@@ -144,9 +158,9 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   x.kmax = q_last;
   x.np = 0;
   x.a0 = (x.kmin / 16) * 16;
-  if (x.kmin < x.P) x.np = (x.P - x.a0 + 63) / 64;
-  const int cfirst = max(x.kmin, x.P);
-  x.c0 = x.P + ((cfirst - x.P) / 64) * 64;
+  if (x.kmin < x.Pk) x.np = (x.Pk - x.a0 + 63) / 64;
+  const int cfirst = max(x.kmin, x.Pk);
+  x.c0 = x.Pk + ((cfirst - x.Pk) / 64) * 64;
   x.nc = (x.kmax >= x.c0) ? (x.kmax - x.c0) / 64 + 1 : 0;
   x.rot = x.np > 1 ? static_cast<int>((blockIdx.x * 2u + x.ds) * 5u % static_cast<unsigned>(x.np)) : 0;
   return true;
@@ -243,7 +257,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       PageRef r{-1, 0};
       if (j < nt && x.prefix(j) && lane < 4) {
         const int pos = x.start(j) + 16 * lane;   // a 16-row group lies in one page
-        if (pos < x.P) {
+        if (pos < x.Pk) {
           const int q = pos / p.page_size;
           r.off = pos - q * p.page_size;
           r.pid = ld_nc_early(bt + q);
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       TileSrc ts;
       const int st0 = x.start(j);
       ts.prefix = x.prefix(j);
-      ts.lim = ts.prefix ? x.P - st0 : x.n - (st0 - x.P);
+      ts.lim = ts.prefix ? x.Pk - st0 : x.n - (st0 - x.P);
       ts.bgroup = (ts.prefix && ts.lim < 64 && (ts.lim & 15) != 0) ? (ts.lim >> 4) : -1;
       ts.tok0 = x.qo0 + st0 - x.P;
       // lane g < 4 resolves group g's slab row; a bad page id reads as zeros
@@ -512,7 +526,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         uint32_t sr[32];
         tmem_ld32(trow + s_col + 32 * half, sr);
         tmem_ld_wait();
-        const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.P - 1) : qpos);
+        const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.Pk - 1) : qpos);
         const int clo = klo - st0, chi = khi - st0;
         if (__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {   // all 32 columns visible to the warp's rows
 #pragma unroll
@@ -644,6 +658,8 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
   k.num_tokens = a.num_tokens;
   k.qo_indptr = a.qo_indptr;
   k.prefix_lens = a.prefix_lens;
+  k.seq_lens = a.seq_lens;
+  k.keys_in_pages = a.keys_in_pages;
   k.block_table = a.block_table;
   k.out = static_cast<__nv_bfloat16*>(a.out);
   k.lse = a.lse;

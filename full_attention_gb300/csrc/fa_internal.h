@@ -151,6 +151,7 @@ struct ExtendArgs {
   const void* v_ext;
   const int32_t* qo_indptr;
   const int32_t* prefix_lens;
+  const int32_t* seq_lens;   // keys_in_pages: lengths including the new tokens
   const int32_t* block_table;
   const void* k_slab;
   const void* v_slab;
@@ -164,6 +165,7 @@ struct ExtendArgs {
   float* lse;
   int B, Hq, Hkv, D, kind, window, page_size, num_pages, max_pages_per_seq, max_q_len,
       max_prefix_len, kv_dtype, num_tokens, early_metadata;
+  int keys_in_pages;   // 1: every key from the slab (new tokens already stored), no k_ext / v_ext
   float sm_scale;
   unsigned int* err;
   // per-call maps: q as (64-column block, head, token, block index) boxes of

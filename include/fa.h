@@ -338,6 +338,27 @@ FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void
                                int32_t max_q_len, int32_t max_prefix_len, void* out, float* lse,
                                void* stream);
 
+/* Decode of n_b >= 1 new tokens per sequence whose k, v rows are already
+ * stored: the verification step of speculative decoding, whose drafted
+ * tokens attend over the target's paged cache ("FreeToken PR #898",
+ * description: the assistant draft of speculative decoding reads the
+ * target's slabs).
+ * Query i of sequence b sits at position seq_lens[b] - n_b + i and attends
+ * to keys [lo, its position] of the layer's regime (causal; sliding adds
+ * q_pos - kv_pos < W), every key read from the slab through the block table.
+ * The extend kernel computes it, with the chunk's keys taken from the slab.
+ * q: bf16 [num_tokens][Hq][D], qo_indptr: int32 [B + 1] (device; n_b =
+ * qo_indptr[b+1] - qo_indptr[b] <= max_q_len), seq_lens: int32 [B] (device;
+ * lengths including the new tokens, <= max_seq_len; a length below n_b sets
+ * FA_DEV_ERR_BOUND), block_table: int32 [B][max_pages_per_seq].  out: bf16
+ * [num_tokens][Hq][D]; lse: optional float [num_tokens][Hq].  bf16 slabs
+ * only (int8: FA_ERR_UNSUPPORTED); Hq / Hkv must divide 128. */
+FA_API fa_status fa_paged_decode_multi_attn(fa_cache* cache, int32_t layer, const void* q, const int32_t* qo_indptr,
+                                            const int32_t* seq_lens, const int32_t* block_table,
+                                            int32_t max_pages_per_seq, int32_t B, int32_t num_tokens,
+                                            int32_t max_q_len, int32_t max_seq_len, void* out, float* lse,
+                                            void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device (FA_DEV_ERR_* bits; 0 = no error). */
 FA_API fa_status fa_get_device_error(int32_t* code, void* stream);
