@@ -49,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "fa_cache_create": (i32, [ctypes.POINTER(LayerDesc), i32, i32, i32, i32, ctypes.POINTER(vp)]),
         "fa_cache_destroy": (None, [vp]),
         "fa_cache_set_flags": (i32, [vp, ctypes.c_uint32]),
+        "fa_cache_set_window_pool": (i32, [vp, i32]),
         "fa_cache_layer_source": (i32, [vp, i32, ctypes.POINTER(i32)]),
         "fa_cache_slab_bytes": (i32, [vp, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "fa_cache_bind_slab": (i32, [vp, i32, vp, vp, vp, vp]),
@@ -121,6 +122,7 @@ class Cache:
     def __init__(self, layers, num_pages: int, page_size: int, kv_dtype: int = KV_BF16):
         self.layers = [dict(d) for d in layers]
         self.num_pages, self.page_size, self.kv_dtype = int(num_pages), int(page_size), int(kv_dtype)
+        self.window_pages = 0
         arr = (LayerDesc * len(layers))(*[_desc(d) for d in layers])
         h = ctypes.c_void_p()
         _check(_lib.fa_cache_create(arr, len(layers), self.num_pages, self.page_size, self.kv_dtype,
@@ -138,6 +140,18 @@ class Cache:
         """FA_FLAG_* options; FLAG_EARLY_METADATA lets kernels read index
         arrays before the previous kernel in the stream has finished."""
         _check(_lib.fa_cache_set_flags(self._h, int(flags)))
+
+    def set_window_pool(self, window_pages: int) -> None:
+        """fa_cache_set_window_pool: the sliding layers' slabs get a pool of
+        their own (before binding them)."""
+        _check(_lib.fa_cache_set_window_pool(self._h, int(window_pages)))
+        self.window_pages = int(window_pages)
+
+    def layer_pages(self, layer: int) -> int:
+        """Pages in the slab the layer reads."""
+        if self.layers[layer]["kind"] == SLIDING and self.window_pages > 0:
+            return self.window_pages
+        return self.num_pages
 
     def source(self, layer: int) -> int:
         out = ctypes.c_int32()
@@ -163,7 +177,7 @@ class Cache:
         for i, d in enumerate(self.layers):
             if self.source(i) != i:
                 continue
-            shape = (self.num_pages, d["num_kv_heads"], self.page_size, d["head_dim"])
+            shape = (self.layer_pages(i), d["num_kv_heads"], self.page_size, d["head_dim"])
             dt = torch.int8 if self.kv_dtype == KV_INT8 else torch.bfloat16
             k = torch.empty(shape, dtype=dt, device=device)
             v = torch.empty(shape, dtype=dt, device=device)

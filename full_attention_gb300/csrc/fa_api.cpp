@@ -315,6 +315,21 @@ fa_status fa_cache_set_flags(fa_cache* c, uint32_t flags) {
   return ok();
 }
 
+fa_status fa_cache_set_window_pool(fa_cache* c, int32_t window_pages) {
+  if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
+  if (window_pages < 0) return fail(FA_ERR_INVALID_ARG, "window_pages must be >= 0");
+  for (size_t i = 0; i < c->layers.size(); ++i) {
+    const Layer& L = c->layers[i];
+    if (L.d.kind != FA_SLIDING) continue;
+    if (c->slabs[i].bound) return fail(FA_ERR_INVALID_ARG, "set the window pool before binding sliding slabs (layer %zu is bound)", i);
+    const int64_t pages = window_pages > 0 ? window_pages : c->num_pages;
+    if (pages * L.d.num_kv_heads * c->page_size >= (1LL << 31))
+      return fail(FA_ERR_UNSUPPORTED, "layer %zu: window_pages * Hkv * page_size must stay below 2^31", i);
+  }
+  c->window_pages = window_pages;
+  return ok();
+}
+
 fa_status fa_cache_layer_source(const fa_cache* c, int32_t layer, int32_t* slab_owner) {
   fa_status st = check_layer(c, layer);
   if (st) return st;
@@ -332,7 +347,7 @@ fa_status fa_cache_slab_bytes(const fa_cache* c, int32_t layer, size_t* kv_bytes
     *kv_bytes = *scale_bytes = 0;
     return ok();
   }
-  const size_t rows = static_cast<size_t>(c->num_pages) * L.d.num_kv_heads * c->page_size;
+  const size_t rows = static_cast<size_t>(layer_pages(c, layer)) * L.d.num_kv_heads * c->page_size;
   *kv_bytes = rows * L.d.head_dim * elem_bytes(c->kv_dtype);
   *scale_bytes = c->kv_dtype == FA_KV_INT8 ? rows * sizeof(float) : 0;
   return ok();
@@ -353,7 +368,7 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
       return fail(FA_ERR_INVALID_ARG, "layer %d: scales must be 16-byte aligned", layer);
   }
   Slab& s = c->slabs[layer];
-  const uint64_t rows = static_cast<uint64_t>(c->num_pages) * L.d.num_kv_heads * c->page_size;
+  const uint64_t rows = static_cast<uint64_t>(layer_pages(c, layer)) * L.d.num_kv_heads * c->page_size;
   st = encode_slab_map(&s.tm_k, k, L.d.head_dim, c->kv_dtype, rows);
   if (st) return st;
   st = encode_slab_map(&s.tm_v, v, L.d.head_dim, c->kv_dtype, rows);
@@ -403,7 +418,7 @@ fa_status fa_kv_store(fa_cache* c, int32_t layer, const void* k, const void* v, 
   unsigned int* err = device_error_word(&ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   StoreArgs a{k, v, slot_mapping, s->k, s->v, s->k_scale, s->v_scale, T, L.d.num_kv_heads, L.d.head_dim,
-              c->page_size, c->num_pages, c->kv_dtype, (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0, err};
+              c->page_size, layer_pages(c, layer), c->kv_dtype, (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0, err};
   ce = launch_store(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "store launch: %s", cudaGetErrorString(ce));
   return ok();
@@ -437,7 +452,7 @@ fa_status fa_kv_store_layers(fa_cache* c, int32_t n, const int32_t* layers, cons
     if (!k[i] || !v[i] || !slot_mapping[i]) return fail(FA_ERR_INVALID_ARG, "k, v, slot_mapping of layer %d must be non-NULL", layers[i]);
     if (!aligned16(k[i]) || !aligned16(v[i])) return fail(FA_ERR_INVALID_ARG, "k, v of layer %d must be 16-byte aligned", layers[i]);
     a[m++] = StoreArgs{k[i], v[i], slot_mapping[i], s->k, s->v, s->k_scale, s->v_scale, T, L.d.num_kv_heads,
-                       L.d.head_dim, c->page_size, c->num_pages, c->kv_dtype,
+                       L.d.head_dim, c->page_size, layer_pages(c, layers[i]), c->kv_dtype,
                        (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0, err};
   }
   if (m == 0) return ok();
@@ -512,7 +527,7 @@ static void fill_decode_args(DecodeArgs& a, const fa_cache* c, int32_t layer, co
   a.kind = L.d.kind;
   a.window = L.d.window;
   a.page_size = c->page_size;
-  a.num_pages = c->num_pages;
+  a.num_pages = layer_pages(c, layer);
   a.max_pages_per_seq = max_pages_per_seq;
   a.max_seq_len = max_seq_len;
   a.kv_dtype = c->kv_dtype;
@@ -690,7 +705,7 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.kind = L.d.kind;
   a.window = L.d.window;
   a.page_size = c->page_size;
-  a.num_pages = c->num_pages;
+  a.num_pages = layer_pages(c, layer);
   a.max_pages_per_seq = max_pages_per_seq;
   a.max_q_len = max_q_len;
   a.max_prefix_len = max_prefix_len;
@@ -754,7 +769,7 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   a.kind = L.d.kind;
   a.window = L.d.window;
   a.page_size = c->page_size;
-  a.num_pages = c->num_pages;
+  a.num_pages = layer_pages(c, layer);
   a.max_pages_per_seq = max_pages_per_seq;
   a.max_q_len = max_q_len;
   a.max_prefix_len = max_seq_len;   // bounds the sequence lengths in this mode

@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     struct TileSrc {
       int row0[4];   // slab row of each 16-row group (prefix tiles), -1: no page
       int lim;       // rows [0, lim) of the tile hold keys (prefix: < P)
+      int wlim;      // rows below wlim precede every visible key of the CTA (window start): read as zero
       int bgroup;    // the group holding the prefix end inside it, -1: none
       bool prefix;
       int tok0;      // chunk tiles: first token row in k_ext / v_ext
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       ts.lim = ts.prefix ? x.Pk - st0 : x.n - (st0 - x.P);
       ts.bgroup = (ts.prefix && ts.lim < 64 && (ts.lim & 15) != 0) ? (ts.lim >> 4) : -1;
       ts.tok0 = x.qo0 + st0 - x.P;
+      ts.wlim = ts.prefix ? max(0, x.kmin - st0) : 0;
       // lane g < 4 resolves group g's slab row; a bad page id reads as zeros
       int r0 = -1;
       if (lane < 4 && ts.prefix && 16 * lane < ts.lim) {
@@ -308,22 +310,25 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
               int tx = 0;
 #pragma unroll
               for (int g = 0; g < 4; ++g)
-                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim) tx += C::CPS * 2048;
+                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim) tx += C::CPS * 2048;
               mbar_arrive_expect_tx(&full[sl], tx);
 #pragma unroll
               for (int h = 0; h < C::CPS; ++h)
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                  if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim)
+                  if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim)
                     tma_load_3d(dst + h * C::CHUNK + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk0 + h,
                                 ts.row0[g], pol);
             }
-            // groups without a page (or past the prefix) must read as zero: the slot holds older data
+            // groups without a page, past the prefix or before the window start
+            // must read as zero: the slot holds older data, and the slab rows
+            // there may hold anything (NaN included) that the PV MMA would
+            // multiply by a zero weight
             const uint8_t* base = is_v ? p.v_slab : p.k_slab;
             bool any_cp = false;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              const bool tma = g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim;
+              const bool tma = g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
               if (tma) continue;
               any_cp = true;
               // 16 rows x 8 units per block: lane copies rows lane / 8 + 4 i, unit lane % 8
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                   const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
-                  const bool v = ts.row0[g] >= 0 && r < ts.lim;
+                  const bool v = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
                   const uint8_t* src =
                       base + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + (blk0 + h) * 64) * 2 + (lane & 7) * 16 : 0);
                   cp_async16_zfill(dst + h * C::CHUNK + sw128(r, lane & 7), src, v, pol);

@@ -47,13 +47,19 @@ struct Layer {
 struct fa_cache {
   std::vector<fa::Layer> layers;
   std::vector<fa::Slab> slabs;   // indexed by layer; only owners are bound
-  int32_t num_pages = 0;
+  int32_t num_pages = 0;      // pages of each full layer's slab
+  int32_t window_pages = 0;   // pages of each sliding layer's slab (0: num_pages)
   int32_t page_size = 0;
   int32_t kv_dtype = FA_KV_BF16;
   uint32_t flags = 0;   // FA_FLAG_*
 };
 
 namespace fa {
+
+// Pages in the slab a layer reads: sliding layers may have a pool of their own.
+inline int32_t layer_pages(const fa_cache* c, int32_t layer) {
+  return (c->layers[layer].d.kind == FA_SLIDING && c->window_pages > 0) ? c->window_pages : c->num_pages;
+}
 
 // thread-local error message
 fa_status fail(fa_status st, const char* fmt, ...);

@@ -142,6 +142,17 @@ FA_API void fa_cache_destroy(fa_cache* cache);
  * library.  Host only. */
 FA_API fa_status fa_cache_set_flags(fa_cache* cache, uint32_t flags);
 
+/* Give the sliding layers' slabs a page pool of their own (the pages' window
+ * pool: "FreeToken PR #898", description, the window slots come from one
+ * full-to-window index mapping; "pegainfer issue #807", Description, the
+ * sliding group releases pages the full group still reads).  Sliding layers
+ * then hold window_pages pages each (full layers keep num_pages) and their
+ * block tables index that pool: entries for positions outside the window
+ * may be -1 or point at pages since reused, as no kernel reads them.  A page
+ * id >= window_pages in a sliding layer's table sets FA_DEV_ERR_PAGE.  Call
+ * before binding any sliding slab; 0 restores the single pool. */
+FA_API fa_status fa_cache_set_window_pool(fa_cache* cache, int32_t window_pages);
+
 /* Slab owner of `layer`: the layer itself if it owns a slab, else its
  * resolved source.  Host only. */
 FA_API fa_status fa_cache_layer_source(const fa_cache* cache, int32_t layer, int32_t* slab_owner);

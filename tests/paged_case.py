@@ -37,7 +37,7 @@ class DecodeCase:
     current token's k, v stored through the library, then attention per layer."""
 
     def __init__(self, layers, lens, page_size=16, kv_dtype=W.KV_BF16, seed=0, device="cuda",
-                 window_table=False, poison=False, pool_factor=1.25, min_pool=0):
+                 window_table=False, poison=False, pool_factor=1.25, min_pool=0, window_pool=False):
         import full_attention_gb300 as fa
         self.fa = fa
         self.layers = layers
@@ -61,7 +61,16 @@ class DecodeCase:
             self.plans[i] = plan
             num_pages = max(num_pages, plan.num_pages)
         self.num_pages = num_pages
-        self.cache = fa.Cache(layers, num_pages, page_size, kv_dtype)
+        if window_pool:
+            # the sliding layers' tables (in-window pages only) index a pool of their own
+            assert window_table
+            full_pages = [self.plans[i].num_pages for i, d in enumerate(layers) if d["kind"] == W.FULL]
+            win_pages = [self.plans[i].num_pages for i, d in enumerate(layers) if d["kind"] == W.SLIDING]
+            self.num_pages = max(full_pages or [full.num_pages])
+            self.window_pages = max(win_pages)
+        self.cache = fa.Cache(layers, self.num_pages, page_size, kv_dtype)
+        if window_pool:
+            self.cache.set_window_pool(self.window_pages)
         self.src = [self.cache.source(i) for i in range(len(layers))]
         self.slabs = self.cache.allocate(device)
         self.bt_dev = {i: torch.from_numpy(self.plans[i].block_table).to(device) for i in range(len(layers))}
@@ -117,7 +126,7 @@ class DecodeCase:
         """NaN every slab position a query of this layer must not read."""
         k_s, v_s, _, _ = self.slabs[i]
         bt = self.plans[i].block_table
-        mask = torch.ones(self.num_pages, self.ps, dtype=torch.bool)
+        mask = torch.ones(k_s.shape[0], self.ps, dtype=torch.bool)
         for b, L in enumerate(self.lens):
             lo = self._visible_lo(d, int(L))
             for pos in range(lo, int(L)):

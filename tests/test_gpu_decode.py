@@ -215,3 +215,34 @@ def test_early_metadata_flag_gives_identical_results():
     for (a, la), (b, lb) in zip(plain, early):
         assert torch.equal(a, b) and torch.equal(la, lb)
     assert case.fa.device_error() == 0
+
+
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+def test_window_pool(kv_dtype):
+    """Sliding layers on a pool of their own: their tables hold only the
+    in-window pages (-1 elsewhere) and index a pool sized for the windows,
+    while the full layer keeps the big pool; a shared sliding layer reads
+    its source's window-pool slab."""
+    layers = [lay(W.SLIDING, 256, 8, 1, 64), lay(W.FULL, 512, 8, 1), lay(W.SLIDING, 256, 8, 1, 64, W.KV_AUTO)]
+    lens = [3000, 17, 1024, 4500, 65, 2]
+    case = DecodeCase(layers, lens, 16, kv_dtype, seed=15, window_table=True, window_pool=True,
+                      poison=(kv_dtype == W.KV_BF16))
+    assert case.window_pages < case.num_pages // 10
+    assert case.slabs[0][0].shape[0] == case.window_pages and case.slabs[1][0].shape[0] == case.num_pages
+    check_layers(case, range(case.B))
+    # the extend kernel on the same pool: one new token per sequence, keys from the slab
+    q = case.q[0]
+    out = torch.empty_like(q)
+    indptr = torch.arange(0, case.B + 1, dtype=torch.int32, device="cuda")
+    if kv_dtype == W.KV_BF16:
+        case.cache.decode_multi(0, q, indptr, case.lens_dev, case.bt_dev[0], 1, case.max_len, out)
+        ref, _ = case.oracle_decode(0, range(case.B))
+        assert_close(out, ref, what="multi-token decode on the window pool")
+    # a page id past the window pool (not past the full pool) is refused by the sliding layer
+    bt = case.bt_dev[0].clone()
+    L0 = int(case.lens[0])
+    bt[0, (L0 - 1) // 16] = case.window_pages
+    out = torch.empty_like(q)
+    ws = case.workspace(0)
+    case.cache.decode(0, q, bt, case.lens_dev, case.max_len, out, None, ws)
+    assert case.fa.device_error() & case.fa.DEV_ERR_PAGE
