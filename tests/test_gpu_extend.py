@@ -22,7 +22,7 @@ class ExtendCase:
     """One extend call per layer over a paged prefix plus a chunk."""
 
     def __init__(self, layers, prefix, chunk, seed=0, page_size=16, device="cuda", poison_tail=True,
-                 early_metadata=False):
+                 early_metadata=False, poison_window=True):
         import full_attention_gb300 as fa
         self.fa = fa
         self.layers = layers
@@ -45,6 +45,8 @@ class ExtendCase:
             v.copy_(W.randn_bf16(tuple(v.shape), seed * 100 + 11 + 2 * i, device))
             if poison_tail:
                 self._poison(k, v)
+            if poison_window:
+                self._poison_before_window(i, k, v)
         self.indptr = np.concatenate([[0], np.cumsum(self.chunk)]).astype(np.int32)
         self.N = int(self.indptr[-1])
         self.q, self.kx, self.vx = {}, {}, {}
@@ -67,6 +69,22 @@ class ExtendCase:
         mask = torch.zeros(k.shape[0], self.ps, dtype=torch.bool)
         for b in range(self.B):
             for pos in range(int(self.prefix[b]), int(self.prefix[b] + self.chunk[b])):
+                mask[self.bt_np[b, pos // self.ps], pos % self.ps] = True
+        mask = mask.to(self.device)[:, None, :, None].expand_as(k)
+        k.masked_fill_(mask, float("nan"))
+        v.masked_fill_(mask, float("nan"))
+
+    def _poison_before_window(self, o, k, v):
+        """NaN the slots of a sliding slab before every query's window: the
+        first query of sequence b sits at P_b and sees keys > P_b - W.  The
+        page holding P_b - W + 1 is read from its 16-row boundary, so this
+        puts NaN inside a tile the kernel copies."""
+        ws = [d["window"] for j, d in enumerate(self.layers) if self.src[j] == o and d["kind"] == W.SLIDING]
+        if not ws:
+            return
+        mask = torch.zeros(k.shape[0], self.ps, dtype=torch.bool)
+        for b in range(self.B):
+            for pos in range(0, max(0, int(self.prefix[b]) - max(ws) + 1)):
                 mask[self.bt_np[b, pos // self.ps], pos % self.ps] = True
         mask = mask.to(self.device)[:, None, :, None].expand_as(k)
         k.masked_fill_(mask, float("nan"))
