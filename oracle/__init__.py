@@ -9,14 +9,16 @@ seeded generators in ``workloads.py``.
 It computes the plain definitions, slowly and obviously:
 
 * layer map -- which slab a layer reads, and what a token costs in bytes;
-* the paged KV store (a bf16 copy, or int8 per-token-head codes with an fp32
-  scale), computed in fp32 where bit-exactness with the GPU is required;
+* the paged KV store (a bf16 copy, or int8 or fp8 e4m3 per-token-head codes
+  with an fp32 scale), computed in fp32 where bit-exactness with the GPU is
+  required;
 * decode and extend attention over the *logically gathered* KV in float64:
   gather the visible rows through the block table, then softmax(scale q.K) V.
 
 Conventions (the same ones the C boundary documents):
 
-* bf16 values travel as numpy ``uint16`` bit patterns; int8 codes as ``int8``.
+* bf16 values travel as numpy ``uint16`` bit patterns; int8 codes as ``int8``;
+  fp8 e4m3 codes as ``uint8`` bit patterns.
 * slab layout ``[num_pages][Hkv][page_size][D]``; scales ``[num_pages][Hkv][page_size]``.
 * a slot is ``page * page_size + offset``; a negative slot is skipped.
 * query head ``j`` reads KV head ``j // (Hq / Hkv)`` (contiguous groups).
@@ -37,6 +39,7 @@ KV_OWN = -1
 KV_AUTO = -2
 KV_BF16 = 0
 KV_INT8 = 1
+KV_FP8 = 2
 
 
 # ---------------------------------------------------------------------------
@@ -111,8 +114,8 @@ def kv_bytes_per_token(layers, kind: int, kv_dtype: int) -> int:
     """Bytes one token occupies across the slabs of the owning layers of `kind`.
 
     Per owning layer and KV head: K and V rows of head_dim elements (2 bytes in
-    bf16, 1 byte in int8) plus, in the int8 per-token-head format, one fp32
-    scale each for K and V.  Shared layers cost nothing.  ("FreeToken PR #898",
+    bf16, 1 byte in the 8-bit formats) plus, in the int8 and fp8 per-token-head
+    formats, one fp32 scale each for K and V.  Shared layers cost nothing.  ("FreeToken PR #898",
     description bullets on kv_cache_group_specs and the per-token-head formats;
     the "End to end" section prints the resulting unit_bytes.)
     """
@@ -168,11 +171,70 @@ def quantize_int8_per_token_head(x_bits):
     return c.astype(np.int8), s
 
 
-def store_int8(codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping, page_size: int) -> None:
-    """Quantise and write rows like store_bf16, into int8 code slabs
-    [num_pages][Hkv][ps][D] and fp32 scale arrays [num_pages][Hkv][ps]."""
-    ck, sk = quantize_int8_per_token_head(k)
-    cv, sv = quantize_int8_per_token_head(v)
+# fp8 e4m3 ("FreeToken PR #898", description: the fp8_per_token_head format,
+# stored and looked up like the int8 one).  The pages name the format only; the
+# encoding is E4M3 of the OCP 8-bit floating point specification, the variant
+# without infinities, whose largest finite magnitude is 448.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """float64 value of e4m3 bit patterns (uint8).
+
+    Bit 7 is the sign, bits 6..3 an exponent field e with bias 7, bits 2..0 a
+    mantissa m.  e > 0 gives (1 + m/8) * 2**(e - 7); e = 0 gives the subnormal
+    (m/8) * 2**-6.  The patterns 0x7F and 0xFF are NaN; there are no
+    infinities, so 0x7E = 448 is the largest finite magnitude.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where((c & 0x80) != 0, -mag, mag)
+
+
+def e4m3_round(y) -> np.ndarray:
+    """e4m3 codes of float32 values y: the nearest finite e4m3 value, a tie
+    going to the code with the even mantissa, magnitudes above 448
+    saturating to 448.  The sign is kept, so a negative value that rounds to
+    zero gives 0x80.  (Round-to-nearest-even with saturation to the finite
+    range: the plain reading for a quantised cache, which must never hold NaN.)"""
+    y = np.asarray(y, dtype=np.float32)
+    mags = e4m3_value(np.arange(0x7F, dtype=np.uint8))   # codes 0 .. 126, ascending
+    a = np.abs(y).astype(np.float64)
+    lo = np.clip(np.searchsorted(mags, a, side="right") - 1, 0, 126)   # mags[lo] <= a
+    hi = np.minimum(lo + 1, 126)
+    d_lo = a - mags[lo]
+    d_hi = mags[hi] - a
+    up = (hi > lo) & ((d_hi < d_lo) | ((d_hi == d_lo) & (lo % 2 == 1)))
+    code = np.where(up, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(y), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def quantize_fp8_per_token_head(x_bits):
+    """fp8 e4m3 per-token-head quantisation of rows x[..., D] (bf16 bits).
+
+    For each row, in fp32 with IEEE round-to-nearest-even: a = max |x_d|,
+    s = a / 448, c_d = e4m3_round(x_d / s); an all-zero row gets s = 0 and
+    codes 0.  Returns (codes uint8 [..., D], scale float32 [...]).  The scale
+    maps the row's largest magnitude onto the largest finite e4m3 value, as
+    the int8 format maps it onto 127.
+    """
+    x = bf16_to_f32(x_bits)
+    a = np.max(np.abs(x), axis=-1).astype(np.float32)
+    s = (a / np.float32(E4M3_MAX)).astype(np.float32)
+    zero = a == np.float32(0.0)
+    s_div = np.where(zero, np.float32(1.0), s).astype(np.float32)
+    q = (x / s_div[..., None]).astype(np.float32)
+    c = np.where(zero[..., None], np.uint8(0), e4m3_round(q))
+    return c.astype(np.uint8), s
+
+
+def _store_quantised(quantize, codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping, page_size: int) -> None:
+    ck, sk = quantize(k)
+    cv, sv = quantize(v)
     for t, slot in enumerate(np.asarray(slot_mapping)):
         slot = int(slot)
         if slot < 0:
@@ -182,6 +244,20 @@ def store_int8(codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping, page_size
         codes_v[page, :, off, :] = cv[t]
         scale_k[page, :, off] = sk[t]
         scale_v[page, :, off] = sv[t]
+
+
+def store_int8(codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping, page_size: int) -> None:
+    """Quantise and write rows like store_bf16, into int8 code slabs
+    [num_pages][Hkv][ps][D] and fp32 scale arrays [num_pages][Hkv][ps]."""
+    _store_quantised(quantize_int8_per_token_head, codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping,
+                     page_size)
+
+
+def store_fp8(codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping, page_size: int) -> None:
+    """Quantise and write rows like store_bf16, into e4m3 code slabs (uint8)
+    [num_pages][Hkv][ps][D] and fp32 scale arrays [num_pages][Hkv][ps]."""
+    _store_quantised(quantize_fp8_per_token_head, codes_k, codes_v, scale_k, scale_v, k, v, slot_mapping,
+                     page_size)
 
 
 # ---------------------------------------------------------------------------
@@ -204,7 +280,8 @@ def visible_keys(q_pos: int, kind: int, window: int) -> tuple:
 def gather_rows(slab, scales, block_table_row, positions, h: int, page_size: int) -> np.ndarray:
     """Logical rows at `positions` of KV head h, as float64 [n][D]: page =
     block_table_row[pos // page_size], offset = pos % page_size.  bf16 slabs
-    (uint16) are widened exactly; int8 slabs are dequantised as code * scale."""
+    (uint16) are widened exactly; int8 slabs (int8) and fp8 slabs (uint8 e4m3
+    bit patterns) are dequantised as value(code) * scale."""
     positions = np.asarray(positions, dtype=np.int64)
     pages = np.asarray(block_table_row, dtype=np.int64)[positions // page_size]
     if np.any(pages < 0):
@@ -214,7 +291,8 @@ def gather_rows(slab, scales, block_table_row, positions, h: int, page_size: int
     if slab.dtype == np.uint16:
         return bf16_to_f64(rows)
     sc = scales[pages, h, offs].astype(np.float64)
-    return rows.astype(np.float64) * sc[:, None]
+    vals = e4m3_value(rows) if slab.dtype == np.uint8 else rows.astype(np.float64)
+    return vals * sc[:, None]
 
 
 def softmax_attention(q, K, V, sm_scale: float):

@@ -8,7 +8,10 @@
   softmax rows sum to 1, chunked == one-shot extend, decode == extend row,
   sliding != full once L > W);
 * the per-token byte counts, slab counts, sources and ratios the pages print;
-* int8 codes against exact rational rounding and hand-worked ties.
+* int8 codes against exact rational rounding and hand-worked ties;
+* fp8 e4m3 codes against hand-worked values and ties, torch's float8_e4m3fn
+  cast (a library routine), and a value table built here from the format's
+  definition with exact rationals.
 
 A planted-mistake test at the end checks that plausible slips in the oracle
 (window off by one, scale dropped, page offset misread, K and V swapped) make
@@ -432,6 +435,216 @@ def test_int8_zero_row_and_store():
 
 
 # ---------------------------------------------------------------------------
+# fp8 e4m3 pins
+# ---------------------------------------------------------------------------
+
+def e4m3_table_exact():
+    """Every finite non-negative e4m3 value as an exact rational, by code,
+    built from the format's definition (bias 7, 3 mantissa bits, exponent 0
+    subnormal, code 0x7F NaN)."""
+    out = {}
+    for code in range(0x7F):
+        e, m = code >> 3, code & 7
+        out[code] = Fraction(m, 8) * Fraction(1, 64) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+    return out
+
+
+def e4m3_nearest_exact(y: Fraction) -> int:
+    """Code of the e4m3 value nearest to the rational y (ties: even code),
+    saturating at 448, sign kept (y = 0 is taken as +0)."""
+    table = e4m3_table_exact()
+    a = abs(y)
+    best = min(table, key=lambda c: (abs(table[c] - a), c & 1))
+    if a >= 448:
+        best = 0x7E
+    return best | (0x80 if y < 0 else 0)
+
+
+def fp8_pin_golden_codes(orc):
+    rows = read_golden("e4m3_codes.txt")
+    y = np.array([float(r[0]) for r in rows], np.float32)
+    want = [int(r[1], 16) for r in rows]
+    assert orc.e4m3_round(y).tolist() == want
+    finite = [c for c in want if (c & 0x7F) != 0x7F]
+    assert np.all(np.isfinite(orc.e4m3_value(np.array(finite, np.uint8))))
+    assert orc.e4m3_value(np.array([0x7E], np.uint8))[0] == 448.0
+    assert orc.e4m3_value(np.array([0x01], np.uint8))[0] == 2.0 ** -9
+    assert np.isnan(orc.e4m3_value(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def fp8_pin_value_table(orc):
+    table = e4m3_table_exact()
+    codes = np.arange(256, dtype=np.uint8)
+    v = orc.e4m3_value(codes)
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            assert np.isnan(v[c])
+            continue
+        want = table[c & 0x7F] * (-1 if c & 0x80 else 1)
+        assert Fraction(float(v[c])) == want, hex(c)
+    # every finite code survives value -> code (including -0 = 0x80)
+    finite = codes[(codes & 0x7F) != 0x7F]
+    assert np.array_equal(orc.e4m3_round(orc.e4m3_value(finite).astype(np.float32)), finite)
+
+
+def fp8_pin_rounding_exact(orc, seed=31):
+    """Random fp32 values across every binade, the exact midpoints between
+    neighbouring codes, and their fp32 neighbours: codes equal the nearest
+    exact e4m3 value (ties even)."""
+    rng = np.random.default_rng(seed)
+    table = e4m3_table_exact()
+    mids = [float((table[c] + table[c + 1]) / 2) for c in range(126)]
+    ys = [np.float32(m) for m in mids]
+    ys += [np.nextafter(np.float32(m), np.float32(np.inf)) for m in mids]
+    ys += [np.nextafter(np.float32(m), np.float32(0)) for m in mids]
+    ys += list((rng.standard_normal(400) * np.exp2(rng.integers(-12, 10, 400))).astype(np.float32))
+    ys += [np.float32(460.0), np.float32(-1e6), np.float32(464.0)]
+    y = np.array(ys, np.float32)
+    y = np.concatenate([y, -y])
+    got = orc.e4m3_round(y)
+    for yi, gi in zip(y, got):
+        assert int(gi) == e4m3_nearest_exact(Fraction(float(yi))) or (yi == 0 and int(gi) in (0, 0x80)), (yi, gi)
+
+
+def fp8_pin_quantized_row_golden(orc):
+    g = {r[0]: r[1:] for r in read_golden("fp8_row.txt")}
+    x = np.array([float(t) for t in g["x"]], np.float32)
+    bits = f32_to_bf16_bits(x)
+    assert np.array_equal(bits_to_f64(bits), x.astype(np.float64))   # all exact in bf16
+    c, s = orc.quantize_fp8_per_token_head(bits[None])
+    assert float(s[0]) == float(g["scale"][0])
+    assert c[0].tolist() == [int(t, 16) for t in g["codes"]]
+
+
+def fp8_pin_quantized_rows_exact(orc, seed=32):
+    """Away from ties, fp32 x / fl(a/448) rounds like the exact 448 x / a;
+    the absmax element maps to +-448; the dequantised row is within half an
+    e4m3 spacing of x; zero rows give s = 0 and codes 0."""
+    rng = np.random.default_rng(seed)
+    x = f32_to_bf16_bits(rng.standard_normal((24, 128)).astype(np.float32) * 3.0)
+    x[5] = 0
+    c, s = orc.quantize_fp8_per_token_head(x)
+    xs = bits_to_f64(x)
+    table = e4m3_table_exact()
+    mids = sorted((table[i] + table[i + 1]) / 2 for i in range(126))
+    checked = 0
+    for r in range(x.shape[0]):
+        if r == 5:
+            assert s[r] == 0 and np.all(c[r] == 0)
+            continue
+        a = max(abs(Fraction(float(t))) for t in xs[r])
+        assert float(s[r]) == float(np.float32(np.float32(a) / np.float32(448)))
+        for d in range(x.shape[1]):
+            exact = Fraction(448) * Fraction(float(xs[r, d])) / a
+            if any(abs(abs(exact) - m_) < Fraction(1, 1 << 20) * max(m_, Fraction(1, 1 << 9)) for m_ in mids):
+                continue
+            assert int(c[r, d]) == e4m3_nearest_exact(exact), (r, d)
+            checked += 1
+        assert np.max(np.abs(orc.e4m3_value(c[r]))) == 448.0
+        err = np.abs(xs[r] - orc.e4m3_value(c[r]) * float(s[r]))
+        # half a spacing: 2^-4 relative for normals, 2^-10 absolute (times s) below 2^-6
+        assert np.all(err <= (np.abs(xs[r]) * 2.0 ** -4 + float(s[r]) * 2.0 ** -10) * (1 + 1e-6))
+    assert checked > 0.99 * (x.size - x.shape[1])
+
+
+FP8_PINS = [fp8_pin_golden_codes, fp8_pin_value_table, fp8_pin_rounding_exact, fp8_pin_quantized_row_golden,
+            fp8_pin_quantized_rows_exact]
+
+
+@pytest.mark.parametrize("pin", FP8_PINS, ids=[p.__name__ for p in FP8_PINS])
+def test_fp8_pin(pin):
+    pin(oracle)
+
+
+def test_e4m3_matches_torch_cast():
+    """torch's float8_e4m3fn cast (round to nearest even) on every in-range
+    value class: midpoints, their neighbours, random values, subnormals."""
+    rng = np.random.default_rng(33)
+    mags = oracle.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    mids = (mags[:-1] + mags[1:]) / 2
+    y = np.concatenate([mids, np.nextafter(mids.astype(np.float32), np.float32(np.inf)),
+                        np.nextafter(mids.astype(np.float32), np.float32(0)), mags,
+                        rng.uniform(-448, 448, 20000), rng.standard_normal(20000) * 2.0 ** -8]).astype(np.float32)
+    y = np.concatenate([y, -y])
+    y = y[np.abs(y) <= 448.0]
+    want = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_round(y), want)
+
+
+def test_fp8_store_and_gather():
+    rng = np.random.default_rng(34)
+    ps, T, H, D, pool = 4, 6, 2, 16, 5
+    k, v = rand_bits(rng, (T, H, D)), rand_bits(rng, (T, H, D))
+    v[4, 0] = 0x8000          # -0.0 everywhere: absmax 0
+    slots = np.array([0, 5, 6, -1, 19, 11], np.int32)
+    ck = np.zeros((pool, H, ps, D), np.uint8)
+    cv = np.zeros_like(ck)
+    sk = np.zeros((pool, H, ps), np.float32)
+    sv = np.zeros_like(sk)
+    oracle.store_fp8(ck, cv, sk, sv, k, v, slots, ps)
+    assert sv[4, 0, 3] == 0 and np.all(cv[4, 0, 3] == 0)
+    bt_row = np.arange(pool, dtype=np.int32)
+    for t, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        p, o = divmod(int(slot), ps)
+        c1, s1 = oracle.quantize_fp8_per_token_head(v[t])
+        assert np.array_equal(cv[p, :, o], c1) and np.array_equal(sv[p, :, o], s1)
+        for h in range(H):
+            got = oracle.gather_rows(ck, sk, bt_row, [slot], h, ps)[0]
+            x = bits_to_f64(k[t, h])
+            assert np.all(np.abs(got - x) <= np.abs(x) * 2.0 ** -4 + sk[p, h, o] * 2.0 ** -10 + 1e-12)
+
+
+def _fp8_mutants():
+    import importlib.util
+
+    def clone():
+        spec = importlib.util.spec_from_file_location("oracle_fp8_mutant", oracle.__file__)
+        m = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(m)
+        return m
+
+    out = {}
+    m = clone()
+    base_round = m.e4m3_round
+
+    def round_ties_away(y):
+        y = np.asarray(y, np.float32)
+        c = base_round(y)
+        # nudge exact ties away from zero
+        up = base_round(np.nextafter(np.abs(y), np.float32(np.inf)) * np.sign(y))
+        mags = m.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+        tie = np.isin(np.abs(y).astype(np.float64), (mags[:-1] + mags[1:]) / 2)
+        return np.where(tie, up, c).astype(np.uint8)
+    m.e4m3_round = round_ties_away
+    out["ties away from zero"] = m
+    m = clone()
+    base_value = m.e4m3_value
+    m.e4m3_value = lambda c: base_value(c) * 2.0
+    out["exponent bias 6"] = m
+    m = clone()
+    m.E4M3_MAX = 240.0
+    out["scale from the e5m2-like range"] = m
+    m = clone()
+    m.e4m3_round = lambda y: base_round(np.abs(np.asarray(y, np.float32)))
+    out["sign dropped"] = m
+    return out
+
+
+@pytest.mark.parametrize("name", list(_fp8_mutants().keys()))
+def test_fp8_planted_mistake_is_caught(name):
+    mutant = _fp8_mutants()[name]
+    failures = 0
+    for pin in FP8_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, IndexError, ValueError):
+            failures += 1
+    assert failures >= 1, f"no fp8 pin caught: {name}"
+
+
+# ---------------------------------------------------------------------------
 # layer map pins (numbers printed by the pages)
 # ---------------------------------------------------------------------------
 
@@ -446,14 +659,16 @@ def e_series(n_layers, period, n_owning, hkv, share=True):
 
 def test_kv_bytes_per_token_golden():
     models = {"E2B": (35, 5, 15, 1), "E4B": (42, 6, 24, 2)}
-    fmt = {"bf16": oracle.KV_BF16, "int8": oracle.KV_INT8}
+    # the page gives one figure for "the 8-bit formats": int8 and fp8 alike
+    fmt = {"bf16": [oracle.KV_BF16], "int8": [oracle.KV_INT8, oracle.KV_FP8]}
     rows = read_golden("kv_bytes_per_token.txt")
     assert len(rows) == 8
     for model, f, sharing, full, window in rows:
         n, per, own, hkv = models[model]
         layers = e_series(n, per, own, hkv, share=(sharing == "after"))
-        assert oracle.kv_bytes_per_token(layers, FULL, fmt[f]) == int(full)
-        assert oracle.kv_bytes_per_token(layers, SLIDING, fmt[f]) == int(window)
+        for kd in fmt[f]:
+            assert oracle.kv_bytes_per_token(layers, FULL, kd) == int(full)
+            assert oracle.kv_bytes_per_token(layers, SLIDING, kd) == int(window)
 
 
 def test_slab_counts_sources_and_ratios():
