@@ -50,8 +50,8 @@ def visible(L, d):
 def decode_bytes(d, lens, kv_dtype):
     """Bytes a decode launch must move: K and V rows of every visible key
     (plus the fp32 scales in int8), the queries, the bf16 outputs and lse."""
-    elem = 1 if kv_dtype == W.KV_INT8 else 2
-    per_tok = d["num_kv_heads"] * 2 * (d["head_dim"] * elem + (4 if kv_dtype == W.KV_INT8 else 0))
+    q8 = kv_dtype != W.KV_BF16   # int8 / fp8: one byte per element plus an fp32 scale per row
+    per_tok = d["num_kv_heads"] * 2 * (d["head_dim"] * (1 if q8 else 2) + (4 if q8 else 0))
     kv = sum(visible(L, d) for L in lens) * per_tok
     B = len(lens)
     qo = B * d["num_q_heads"] * (2 * d["head_dim"] * 2 + 4)
@@ -60,8 +60,8 @@ def decode_bytes(d, lens, kv_dtype):
 
 def store_bytes(d, B, kv_dtype):
     row_in = d["num_kv_heads"] * d["head_dim"] * 2
-    row_out = d["num_kv_heads"] * (d["head_dim"] * (1 if kv_dtype == W.KV_INT8 else 2) +
-                                   (4 if kv_dtype == W.KV_INT8 else 0))
+    q8 = kv_dtype != W.KV_BF16
+    row_out = d["num_kv_heads"] * (d["head_dim"] * (1 if q8 else 2) + (4 if q8 else 0))
     return B * 2 * (row_in + row_out) + B * 4
 
 
@@ -197,7 +197,7 @@ class DecodeStep:
                 k.copy_(W.randn_bf16(tuple(k.shape), s0 + 2 * i, device))
                 v.copy_(W.randn_bf16(tuple(v.shape), s0 + 2 * i + 1, device))
             else:
-                self._fill_int8(i, s0)
+                self._fill_8bit(i, s0)
         self.bt = {i: torch.from_numpy(t).to(device) for i, t in self.tables.items()}
         self.lens_dev = torch.from_numpy(self.lens).to(device)
         self.q, self.out, self.lse, self.ws = {}, {}, {}, {}
@@ -230,7 +230,7 @@ class DecodeStep:
             sum(qo[i] for i in range(len(self.layers)) if self.src[i] != i) + self.store_bytes
         torch.cuda.synchronize()
 
-    def _fill_int8(self, i, s0):
+    def _fill_8bit(self, i, s0):
         torch = self.torch
         d = self.layers[i]
         slots = []
@@ -373,7 +373,7 @@ def gpu_arm(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_max * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.kv_dtype == W.KV_BF16 else "int8",
+        "dtype": {W.KV_BF16: "bf16", W.KV_INT8: "int8", W.KV_FP8: "fp8"}[w.kv_dtype],
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": w.name, "batch": step.B, "layers": nl, "page_size": w.page_size,
                    "max_ctx": step.max_len, "l2": "flushed before every step (256 MiB write)",
@@ -671,10 +671,15 @@ def _oracle_worker(conn, name, units, seed):
         shape = (npg, d["num_kv_heads"], ps, d["head_dim"])
         if w.kv_dtype == W.KV_BF16:
             slab = (_bf16_normal(r, shape), _bf16_normal(r, shape))
-        else:
+        elif w.kv_dtype == W.KV_INT8:
             sc = (r.random(shape[:3], dtype=np.float32) * 0.03).astype(np.float32)
             slab = (r.integers(-127, 128, size=shape, dtype=np.int8), r.integers(-127, 128, size=shape, dtype=np.int8),
                     sc, sc.copy())
+        else:
+            # e4m3 codes: any byte but the two NaN patterns
+            sc = (r.random(shape[:3], dtype=np.float32) * 0.01).astype(np.float32)
+            codes = [r.integers(0, 254, size=shape, dtype=np.uint8) for _ in range(2)]
+            slab = tuple(np.where(c >= 0x7F, c + 1, c).astype(np.uint8) for c in codes) + (sc, sc.copy())
         q = _bf16_normal(r, (1, d["num_q_heads"], d["head_dim"]))
         data.append((d, slab, q, np.arange(npg, dtype=np.int32)[None], np.array([L], np.int32),
                      decode_bytes(d, [L], w.kv_dtype)))
@@ -790,7 +795,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="e2b_decode", choices=["e2b_decode", "long_decode", "int8_decode",
-                                                                  "tiny_decode"])
+                                                                  "fp8_decode", "tiny_decode"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

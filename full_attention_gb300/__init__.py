@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
 
 FULL, SLIDING = 0, 1
-KV_BF16, KV_INT8 = 0, 1
+KV_BF16, KV_INT8, KV_FP8 = 0, 1, 2
 KV_OWN, KV_AUTO = -1, -2
 DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE = 1, 2, 4, 8, 16
 
@@ -178,11 +178,12 @@ class Cache:
             if self.source(i) != i:
                 continue
             shape = (self.layer_pages(i), d["num_kv_heads"], self.page_size, d["head_dim"])
-            dt = torch.int8 if self.kv_dtype == KV_INT8 else torch.bfloat16
+            # fp8 e4m3 codes are held as raw bytes (uint8 bit patterns)
+            dt = {KV_BF16: torch.bfloat16, KV_INT8: torch.int8, KV_FP8: torch.uint8}[self.kv_dtype]
             k = torch.empty(shape, dtype=dt, device=device)
             v = torch.empty(shape, dtype=dt, device=device)
             ks = vs = None
-            if self.kv_dtype == KV_INT8:
+            if self.kv_dtype != KV_BF16:
                 ks = torch.empty(shape[:3], dtype=torch.float32, device=device)
                 vs = torch.empty(shape[:3], dtype=torch.float32, device=device)
             self.bind(i, k, v, ks, vs)

@@ -44,7 +44,9 @@ int sm_count() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static size_t elem_bytes(int kv_dtype) { return kv_dtype == FA_KV_INT8 ? 1 : 2; }
+// int8 and fp8 slabs: one code byte per element plus an fp32 scale per row
+static bool quantised(int kv_dtype) { return kv_dtype != FA_KV_BF16; }
+static size_t elem_bytes(int kv_dtype) { return quantised(kv_dtype) ? 1 : 2; }
 
 // ----------------------------------------------------------------- planning
 DecodePlan plan_decode(const fa_cache* c, int layer, int B, int max_seq_len, long long max_cta) {
@@ -116,7 +118,7 @@ static fa_status encode_slab_map(CUtensorMap* tm, void* base, int D, int kv_dtyp
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(D * eb)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), 1, static_cast<cuuint32_t>(kTile)};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(tm, kv_dtype == FA_KV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  CUresult r = enc(tm, quantised(kv_dtype) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -138,7 +140,7 @@ static fa_status encode_tile_map(CUtensorMap* tm, void* base, int D, int kv_dtyp
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * eb), 128};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(kTile), static_cast<cuuint32_t>(D / blk)};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(tm, kv_dtype == FA_KV_INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  CUresult r = enc(tm, quantised(kv_dtype) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -250,7 +252,7 @@ fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t
   if (num_pages <= 0) return fail(FA_ERR_INVALID_ARG, "num_pages must be positive");
   if (page_size <= 0 || page_size % kTile != 0 || page_size > 256)
     return fail(FA_ERR_UNSUPPORTED, "page_size %d: must be a multiple of %d, at most 256", page_size, kTile);
-  if (kv_dtype != FA_KV_BF16 && kv_dtype != FA_KV_INT8)
+  if (kv_dtype != FA_KV_BF16 && kv_dtype != FA_KV_INT8 && kv_dtype != FA_KV_FP8)
     return fail(FA_ERR_UNSUPPORTED, "kv_dtype %d unsupported", kv_dtype);
   fa_cache* c = new (std::nothrow) fa_cache();
   if (!c) return fail(FA_ERR_INVALID_ARG, "out of host memory");
@@ -349,7 +351,7 @@ fa_status fa_cache_slab_bytes(const fa_cache* c, int32_t layer, size_t* kv_bytes
   }
   const size_t rows = static_cast<size_t>(layer_pages(c, layer)) * L.d.num_kv_heads * c->page_size;
   *kv_bytes = rows * L.d.head_dim * elem_bytes(c->kv_dtype);
-  *scale_bytes = c->kv_dtype == FA_KV_INT8 ? rows * sizeof(float) : 0;
+  *scale_bytes = quantised(c->kv_dtype) ? rows * sizeof(float) : 0;
   return ok();
 }
 
@@ -362,8 +364,8 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
                 L.owner);
   if (!k || !v) return fail(FA_ERR_INVALID_ARG, "layer %d: k and v must be non-NULL", layer);
   if (!aligned16(k) || !aligned16(v)) return fail(FA_ERR_INVALID_ARG, "layer %d: k, v must be 16-byte aligned", layer);
-  if (c->kv_dtype == FA_KV_INT8) {
-    if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "layer %d: int8 format needs k_scale and v_scale", layer);
+  if (quantised(c->kv_dtype)) {
+    if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "layer %d: the 8-bit formats need k_scale and v_scale", layer);
     if (!aligned16(k_scale) || !aligned16(v_scale))
       return fail(FA_ERR_INVALID_ARG, "layer %d: scales must be 16-byte aligned", layer);
   }
@@ -375,7 +377,7 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
   if (st) return st;
   if ((st = encode_tile_map(&s.tm_kt, k, L.d.head_dim, c->kv_dtype, rows))) return st;
   if ((st = encode_tile_map(&s.tm_vt, v, L.d.head_dim, c->kv_dtype, rows))) return st;
-  if (c->kv_dtype == FA_KV_INT8) {
+  if (quantised(c->kv_dtype)) {
     if ((st = encode_scale_map(&s.tm_ks, k_scale, rows))) return st;
     if ((st = encode_scale_map(&s.tm_vs, v_scale, rows))) return st;
   } else {
@@ -384,8 +386,8 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
   }
   s.k = k;
   s.v = v;
-  s.k_scale = c->kv_dtype == FA_KV_INT8 ? k_scale : nullptr;
-  s.v_scale = c->kv_dtype == FA_KV_INT8 ? v_scale : nullptr;
+  s.k_scale = quantised(c->kv_dtype) ? k_scale : nullptr;
+  s.v_scale = quantised(c->kv_dtype) ? v_scale : nullptr;
   s.bound = true;
   return ok();
 }
@@ -396,7 +398,7 @@ size_t fa_kv_bytes_per_token(const fa_cache* c, int32_t kind) {
   for (size_t i = 0; i < c->layers.size(); ++i) {
     const Layer& L = c->layers[i];
     if (L.owner != static_cast<int>(i) || L.d.kind != kind) continue;
-    const size_t row = c->kv_dtype == FA_KV_INT8 ? L.d.head_dim + sizeof(float) : 2 * L.d.head_dim;
+    const size_t row = quantised(c->kv_dtype) ? L.d.head_dim + sizeof(float) : 2 * L.d.head_dim;
     total += 2 * L.d.num_kv_heads * row;
   }
   return total;
@@ -668,7 +670,7 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   if (128 % g != 0)
     return fail(FA_ERR_UNSUPPORTED, "extend packs Hq/Hkv = %d query heads into 128-row tiles; it must divide 128", g);
   if (c->kv_dtype != FA_KV_BF16)
-    return fail(FA_ERR_UNSUPPORTED, "extend over the int8 per-token-head format is not built");
+    return fail(FA_ERR_UNSUPPORTED, "extend over the 8-bit per-token-head formats is not built");
   const Slab* s = nullptr;
   if ((st = check_bound(c, layer, &s))) return st;
   if (!q || !k_ext || !v_ext || !qo_indptr || !prefix_lens || !out || (max_prefix_len > 0 && !block_table))
@@ -735,7 +737,7 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   if (128 % g != 0)
     return fail(FA_ERR_UNSUPPORTED, "multi-token decode packs Hq/Hkv = %d query heads into 128-row tiles; it must divide 128", g);
   if (c->kv_dtype != FA_KV_BF16)
-    return fail(FA_ERR_UNSUPPORTED, "multi-token decode over the int8 per-token-head format is not built");
+    return fail(FA_ERR_UNSUPPORTED, "multi-token decode over the 8-bit per-token-head formats is not built");
   const Slab* s = nullptr;
   if ((st = check_bound(c, layer, &s))) return st;
   if (!q || !qo_indptr || !seq_lens || !block_table || !out) return fail(FA_ERR_INVALID_ARG, "a required pointer is NULL");

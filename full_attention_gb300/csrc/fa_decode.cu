@@ -22,16 +22,17 @@
 //   O^T (D x 8 heads)       += V^T (D x 16) . P^T (16 x 8)
 // with keys on the MMA M side, so 8 query heads fill N exactly and each KV
 // byte is read from HBM once for the whole group.  Warp 4 is a TMA producer:
-// it streams K and V tiles (and int8 scales) into a 3-stage ring of
+// it streams K and V tiles (and 8-bit scales) into a 3-stage ring of
 // 128-byte-swizzled shared-memory tiles, and each segment's queries by a bulk
 // copy.  Warps 0-3 split the QK^T contraction over columns, exchange partial
 // scores through shared memory, run the online softmax redundantly (each lane
 // owns one head) and each accumulate a quarter of O's columns.
 //
-// bf16 slabs use bf16 MMAs.  int8 slabs: codes become exact fp16 integers
-// (byte permute + one subtraction), the K scale multiplies the fp32 scores,
-// the V scale is folded into P (normalised by the step's largest scale, which
-// joins the running rescale), and the MMAs run in fp16.
+// bf16 slabs use bf16 MMAs.  int8 and fp8 slabs: codes become exact fp16
+// values (int8: byte permute + one subtraction; e4m3: the hardware pair
+// conversion), the K scale multiplies the fp32 scores, the V scale is folded
+// into P (normalised by the step's largest scale, which joins the running
+// rescale), and the MMAs run in fp16.
 #include <cfloat>
 #include <climits>
 #include <mutex>
@@ -132,6 +133,21 @@ __device__ __forceinline__ uint32_t i8pair_to_f16x2(uint32_t biased, uint32_t se
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// f16x2 of code bytes I (lower half) and J (upper half) of `raw`: int8 codes
+// or fp8 e4m3 codes, both exact in f16 (e4m3's 3-bit mantissa and its range
+// 2^-9 .. 448 lie inside f16's normal numbers).
+template <int KV, int I, int J>
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t raw) {
+  if constexpr (KV == FA_KV_INT8) {
+    return i8pair_to_f16x2(raw ^ 0x80808080u, I | 0x40u | (J << 8) | 0x4000u);
+  } else {
+    const uint32_t two = (I == 0 && J == 1) ? (raw & 0xffffu)
+                         : (I == 2 && J == 3) ? (raw >> 16) : __byte_perm(raw, 0u, I | (J << 4));
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  }
+}
+
 // Exclusive block scan over all threads of the block; *total gets the sum.
 __device__ __forceinline__ int block_excl_scan(int v, int* sm, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -189,13 +205,9 @@ __device__ __forceinline__ void store_current(const DecK& p, const RowRegs<D>& r
     return;
   }
   const size_t row = (static_cast<size_t>(page) * p.Hkv + h) * p.page_size + off;
-  if constexpr (KV) {
-    row_store_int8<D>(rk, reinterpret_cast<int8_t*>(p.kb) + row * D, p.ksb + row, lane);
-    row_store_int8<D>(rv, reinterpret_cast<int8_t*>(p.vb) + row * D, p.vsb + row, lane);
-  } else {
-    row_store_bf16<D>(rk, reinterpret_cast<__nv_bfloat16*>(p.kb) + row * D, lane);
-    row_store_bf16<D>(rv, reinterpret_cast<__nv_bfloat16*>(p.vb) + row * D, lane);
-  }
+  constexpr size_t elem = KV == FA_KV_BF16 ? 2 : 1;
+  row_store<D, KV>(rk, p.kb + row * D * elem, KV == FA_KV_BF16 ? nullptr : p.ksb + row, lane);
+  row_store<D, KV>(rv, p.vb + row * D * elem, KV == FA_KV_BF16 ? nullptr : p.vsb + row, lane);
 }
 
 template <int D, int KV>
@@ -697,12 +709,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
           } else {
             const int dc = qk_d0 + kk * 32 + (lane >> 4) * 16;
             ldsm_x4(smem_u32(kt + (dc >> 7) * 2048 + sw128(r, (dc & 127) >> 4)), a0, a1, a2, a3);
-            const uint32_t x0 = a0 ^ 0x80808080u, x1 = a1 ^ 0x80808080u;
-            const uint32_t x2 = a2 ^ 0x80808080u, x3 = a3 ^ 0x80808080u;
-            mma_f16(acc, i8pair_to_f16x2(x0, 0x4140), i8pair_to_f16x2(x1, 0x4140), i8pair_to_f16x2(x0, 0x4342),
-                    i8pair_to_f16x2(x1, 0x4342), qf[kk][0], qf[kk][1]);
-            mma_f16(acc1, i8pair_to_f16x2(x2, 0x4140), i8pair_to_f16x2(x3, 0x4140), i8pair_to_f16x2(x2, 0x4342),
-                    i8pair_to_f16x2(x3, 0x4342), qf[kk][2], qf[kk][3]);
+            mma_f16(acc, codes_to_f16x2<KV, 0, 1>(a0), codes_to_f16x2<KV, 0, 1>(a1), codes_to_f16x2<KV, 2, 3>(a0),
+                    codes_to_f16x2<KV, 2, 3>(a1), qf[kk][0], qf[kk][1]);
+            mma_f16(acc1, codes_to_f16x2<KV, 0, 1>(a2), codes_to_f16x2<KV, 0, 1>(a3), codes_to_f16x2<KV, 2, 3>(a2),
+                    codes_to_f16x2<KV, 2, 3>(a3), qf[kk][2], qf[kk][3]);
           }
         }
       }
@@ -795,20 +805,23 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
           o[mt][3] *= fb_;
         }
 
-        if constexpr (!KV) {
+        if constexpr (KV != FA_KV_INT8) {
           // masked keys have p = 0, but their V rows may hold anything (NaN
-          // included): zero this warp's columns of those rows before the MMA
+          // included; e4m3 has NaN codes too, int8 has none): zero this
+          // warp's columns of those rows before the MMA
           if (tile0 * kTile < lo || (tile0 + ntl) * kTile - 1 > qpos) {
-            constexpr int UNITS = C::PV_COLS / 8;   // 16-byte units per row slice
+            constexpr int EPU = 16 / C::ELEM;              // elements per 16-byte unit
+            constexpr int UNITS = C::PV_COLS / EPU;        // 16-byte units per row slice
+            constexpr int EPB = 128 / C::ELEM;             // elements per 128-byte column block
             uint8_t* vw = const_cast<uint8_t*>(vs);
             for (int t = 0; t < ntl; ++t) {
               for (int idx = lane; idx < kTile * UNITS; idx += 32) {
                 const int r = idx / UNITS, uu = idx % UNITS;
                 const int pos = (tile0 + t) * kTile + r;
                 if (pos < lo || pos > qpos) {
-                  const int dc = pv_d0 + uu * 8;
-                  *reinterpret_cast<uint4*>(vw + t * C::TILE_BYTES + (dc >> 6) * 2048 +
-                                            sw128(r, (dc & 63) >> 3)) = make_uint4(0u, 0u, 0u, 0u);
+                  const int dc = pv_d0 + uu * EPU;
+                  *reinterpret_cast<uint4*>(vw + t * C::TILE_BYTES + (dc / EPB) * 2048 +
+                                            sw128(r, (dc % EPB) / EPU)) = make_uint4(0u, 0u, 0u, 0u);
                 }
               }
             }
@@ -837,14 +850,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
               const int dc = pv_d0 + gi2 * 32 + ((lane >> 3) & 1) * 16;
               uint32_t r0, r1, r2, r3;
               ldsm_x4_t(smem_u32(vt + (dc >> 7) * 2048 + sw128(r, (dc & 127) >> 4)), r0, r1, r2, r3);
-              r0 ^= 0x80808080u;
-              r1 ^= 0x80808080u;
-              r2 ^= 0x80808080u;
-              r3 ^= 0x80808080u;
-              mma_f16(o[2 * gi2], i8pair_to_f16x2(r0, 0x4240), i8pair_to_f16x2(r1, 0x4240),
-                      i8pair_to_f16x2(r2, 0x4240), i8pair_to_f16x2(r3, 0x4240), pf[t][0], pf[t][1]);
-              mma_f16(o[2 * gi2 + 1], i8pair_to_f16x2(r0, 0x4341), i8pair_to_f16x2(r1, 0x4341),
-                      i8pair_to_f16x2(r2, 0x4341), i8pair_to_f16x2(r3, 0x4341), pf[t][0], pf[t][1]);
+              mma_f16(o[2 * gi2], codes_to_f16x2<KV, 0, 2>(r0), codes_to_f16x2<KV, 0, 2>(r1),
+                      codes_to_f16x2<KV, 0, 2>(r2), codes_to_f16x2<KV, 0, 2>(r3), pf[t][0], pf[t][1]);
+              mma_f16(o[2 * gi2 + 1], codes_to_f16x2<KV, 1, 3>(r0), codes_to_f16x2<KV, 1, 3>(r1),
+                      codes_to_f16x2<KV, 1, 3>(r2), codes_to_f16x2<KV, 1, 3>(r3), pf[t][0], pf[t][1]);
             }
           }
         }
@@ -1018,11 +1027,15 @@ static DecK make_deck(const DecodeArgs& a) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const DecK k = make_deck(a);
   if (a.kv_dtype == FA_KV_INT8) {
-    if (a.D == 256) return launch_decode_t<256, 1>(a, k, s);
-    return launch_decode_t<512, 1>(a, k, s);
+    if (a.D == 256) return launch_decode_t<256, FA_KV_INT8>(a, k, s);
+    return launch_decode_t<512, FA_KV_INT8>(a, k, s);
   }
-  if (a.D == 256) return launch_decode_t<256, 0>(a, k, s);
-  return launch_decode_t<512, 0>(a, k, s);
+  if (a.kv_dtype == FA_KV_FP8) {
+    if (a.D == 256) return launch_decode_t<256, FA_KV_FP8>(a, k, s);
+    return launch_decode_t<512, FA_KV_FP8>(a, k, s);
+  }
+  if (a.D == 256) return launch_decode_t<256, FA_KV_BF16>(a, k, s);
+  return launch_decode_t<512, FA_KV_BF16>(a, k, s);
 }
 
 cudaError_t launch_decode_layers(const DecodeArgs* a, int n, cudaStream_t s) {
@@ -1039,11 +1052,15 @@ cudaError_t launch_decode_layers(const DecodeArgs* a, int n, cudaStream_t s) {
     m.cta0[i + 1] = m.cta0[i] + a[i].plan.ncta;
   }
   if (a[0].kv_dtype == FA_KV_INT8) {
-    if (a[0].D == 256) return launch_decode_layers_t<256, 1>(m, s);
-    return launch_decode_layers_t<512, 1>(m, s);
+    if (a[0].D == 256) return launch_decode_layers_t<256, FA_KV_INT8>(m, s);
+    return launch_decode_layers_t<512, FA_KV_INT8>(m, s);
   }
-  if (a[0].D == 256) return launch_decode_layers_t<256, 0>(m, s);
-  return launch_decode_layers_t<512, 0>(m, s);
+  if (a[0].kv_dtype == FA_KV_FP8) {
+    if (a[0].D == 256) return launch_decode_layers_t<256, FA_KV_FP8>(m, s);
+    return launch_decode_layers_t<512, FA_KV_FP8>(m, s);
+  }
+  if (a[0].D == 256) return launch_decode_layers_t<256, FA_KV_BF16>(m, s);
+  return launch_decode_layers_t<512, FA_KV_BF16>(m, s);
 }
 
 // ---------------------------------------------------------------------------

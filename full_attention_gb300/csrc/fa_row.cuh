@@ -1,12 +1,15 @@
 // One (token, KV head) row of k or v moved into its slab row by one warp:
-// bf16 copied verbatim, or quantised to the int8 per-token-head format
-// ("FreeToken PR #898", description: one fp32 scale per token and head,
-// codes in [-127, 127]).  Used by the store kernel and by the decode kernel
+// bf16 copied verbatim, or quantised to an 8-bit per-token-head format
+// ("FreeToken PR #898", description: one fp32 scale per token and head;
+// int8 codes in [-127, 127], or fp8 e4m3 codes).  Used by the store kernel and by the decode kernel
 // that stores the current token itself, so both write identical bytes.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
+
+#include "fa.h"
 
 namespace fa {
 
@@ -72,6 +75,49 @@ __device__ __forceinline__ void row_store_int8(const RowRegs<D>& r, int8_t* dst,
     *reinterpret_cast<uint2*>(dst + i * 256 + lane * 8) = make_uint2(packed[0], packed[1]);
   }
   if (lane == 0) *scale = s;
+}
+
+// a = max |x| (fp32), s = a / 448 (IEEE), c = the e4m3 value nearest to the
+// IEEE quotient x / s, ties to the even mantissa, saturating at the largest
+// finite magnitude 448; a = 0 gives s = 0 and all-zero codes.  Same lane
+// layout as row_store_int8.
+template <int D>
+__device__ __forceinline__ void row_store_fp8(const RowRegs<D>& r, uint8_t* dst, float* scale, int lane) {
+  constexpr int NV = RowRegs<D>::NV;
+  float x[NV][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    bf16x8_to_f32(r.v[i], x[i]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = __fdiv_rn(amax, 448.0f);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    uint32_t packed[2] = {0u, 0u};
+    if (amax != 0.0f) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const float2 qv = make_float2(__fdiv_rn(x[i][e], s), __fdiv_rn(x[i][e + 1], s));
+        // element e in the lower byte of the pair
+        const uint32_t pair = __nv_cvt_float2_to_fp8x2(qv, __NV_SATFINITE, __NV_E4M3);
+        packed[e >> 2] |= (pair & 0xffffu) << (8 * (e & 3));
+      }
+    }
+    *reinterpret_cast<uint2*>(dst + i * 256 + lane * 8) = make_uint2(packed[0], packed[1]);
+  }
+  if (lane == 0) *scale = s;
+}
+
+// The slab format's per-row store: KV is the fa_kv_dtype of the slab.
+template <int D, int KV>
+__device__ __forceinline__ void row_store(const RowRegs<D>& r, void* dst, float* scale, int lane) {
+  if constexpr (KV == FA_KV_BF16) row_store_bf16<D>(r, static_cast<__nv_bfloat16*>(dst), lane);
+  else if constexpr (KV == FA_KV_INT8) row_store_int8<D>(r, static_cast<int8_t*>(dst), scale, lane);
+  else row_store_fp8<D>(r, static_cast<uint8_t*>(dst), scale, lane);
 }
 
 }  // namespace fa

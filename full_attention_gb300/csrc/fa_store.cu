@@ -3,9 +3,10 @@
 // dee9371": the store layer writes its post-rotary k, v into its paged cache).
 //
 // One warp moves one (token, KV head, K-or-V) row with 16-byte vector loads
-// and stores.  The int8 per-token-head format quantises the row on the way:
-// a = max|x| (fp32, warp-shuffle reduction), s = a / 127, c = rint(x / s)
-// clamped to [-127, 127], both divisions IEEE round-to-nearest.
+// and stores.  The 8-bit per-token-head formats quantise the row on the way:
+// a = max|x| (fp32, warp-shuffle reduction); int8: s = a / 127, c = rint(x / s)
+// clamped to [-127, 127]; fp8: s = a / 448, c = the e4m3 value nearest x / s,
+// saturating at 448; every division IEEE round-to-nearest.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -62,26 +63,16 @@ __device__ __forceinline__ void store_row(const StoreArgs& a, int warp, int lane
   RowRegs<D> r;
   row_load<D>(r, static_cast<const __nv_bfloat16*>(which ? a.v : a.k) + (static_cast<size_t>(t) * a.Hkv + h) * D, lane);
   const size_t row = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
-  if constexpr (KV) {
-    row_store_int8<D>(r, static_cast<int8_t*>(which ? a.v_slab : a.k_slab) + row * D,
-                      (which ? a.v_scale : a.k_scale) + row, lane);
-  } else {
-    row_store_bf16<D>(r, static_cast<__nv_bfloat16*>(which ? a.v_slab : a.k_slab) + row * D, lane);
-  }
+  constexpr size_t elem = KV == FA_KV_BF16 ? 2 : 1;
+  row_store<D, KV>(r, static_cast<uint8_t*>(which ? a.v_slab : a.k_slab) + row * D * elem,
+                   KV == FA_KV_BF16 ? nullptr : (which ? a.v_scale : a.k_scale) + row, lane);
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) store_bf16_kernel(StoreArgs a) {
+template <int D, int KV>
+__global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
-  store_row<D, 0>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
-}
-
-template <int D>
-__global__ void __launch_bounds__(256) store_int8_kernel(StoreArgs a) {
-  if (!a.early_metadata) griddep_wait();
-  griddep_launch_dependents();
-  store_row<D, 1>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
+  store_row<D, KV>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
 }
 
 // Several layers' stores in one launch: blockIdx.y picks the layer.
@@ -111,8 +102,9 @@ cudaError_t launch_store_layers(const StoreArgs* a, int n, cudaStream_t s) {
   const long grid = (warps * 32 + block - 1) / block;
   if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(grid), static_cast<unsigned>(n)), b(block);
-  if (a[0].kv_dtype == FA_KV_INT8) return launch_pdl(store_layers_kernel<1>, g, b, 0, s, m);
-  return launch_pdl(store_layers_kernel<0>, g, b, 0, s, m);
+  if (a[0].kv_dtype == FA_KV_INT8) return launch_pdl(store_layers_kernel<FA_KV_INT8>, g, b, 0, s, m);
+  if (a[0].kv_dtype == FA_KV_FP8) return launch_pdl(store_layers_kernel<FA_KV_FP8>, g, b, 0, s, m);
+  return launch_pdl(store_layers_kernel<FA_KV_BF16>, g, b, 0, s, m);
 }
 
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {
@@ -122,10 +114,13 @@ cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {
   if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(grid)), b(block);
   if (a.kv_dtype == FA_KV_INT8)
-    return a.D == 256 ? launch_pdl(store_int8_kernel<256>, g, b, 0, s, a)
-                      : launch_pdl(store_int8_kernel<512>, g, b, 0, s, a);
-  return a.D == 256 ? launch_pdl(store_bf16_kernel<256>, g, b, 0, s, a)
-                    : launch_pdl(store_bf16_kernel<512>, g, b, 0, s, a);
+    return a.D == 256 ? launch_pdl(store_kernel<256, FA_KV_INT8>, g, b, 0, s, a)
+                      : launch_pdl(store_kernel<512, FA_KV_INT8>, g, b, 0, s, a);
+  if (a.kv_dtype == FA_KV_FP8)
+    return a.D == 256 ? launch_pdl(store_kernel<256, FA_KV_FP8>, g, b, 0, s, a)
+                      : launch_pdl(store_kernel<512, FA_KV_FP8>, g, b, 0, s, a);
+  return a.D == 256 ? launch_pdl(store_kernel<256, FA_KV_BF16>, g, b, 0, s, a)
+                    : launch_pdl(store_kernel<512, FA_KV_BF16>, g, b, 0, s, a);
 }
 
 }  // namespace fa

@@ -13,8 +13,8 @@
  *                    commit "block mask per attention regime";
  *                    "pegainfer issue #807", Description, second paragraph]
  *
- *   KV-shared layers own no slab: they read the slab (and, in the int8
- *   format, the scales) of their source, the last earlier owning layer of the
+ *   KV-shared layers own no slab: they read the slab (and, in the 8-bit
+ *   formats, the scales) of their source, the last earlier owning layer of the
  *   same attention type, and the store skips them.
  *                   ["FreeToken PR #898: read the source layer's kv slab on
  *                    kv-shared layers", description bullets;
@@ -48,6 +48,8 @@
  *   bf16 slab     K, V: bf16 [num_pages][Hkv][page_size][D]
  *   int8 slab     K, V: int8 [num_pages][Hkv][page_size][D]  (codes)
  *                 k_scale, v_scale: float [num_pages][Hkv][page_size]
+ *   fp8 slab      K, V: uint8 [num_pages][Hkv][page_size][D]  (e4m3 codes)
+ *                 k_scale, v_scale: float [num_pages][Hkv][page_size]
  *   slot          page * page_size + offset; logical position p of sequence b
  *                 lives in page block_table[b][p / page_size], offset
  *                 p % page_size.
@@ -78,7 +80,13 @@ typedef enum {
   FA_ERR_DEVICE = 6         /* reserved for device-side error reports         */
 } fa_status;
 
-typedef enum { FA_KV_BF16 = 0, FA_KV_INT8 = 1 } fa_kv_dtype;
+/* KV slab formats.  The 8-bit per-token-head formats ("FreeToken PR #898",
+ * description: int8_per_token_head and fp8_per_token_head, a shared layer
+ * reading its source's scales) hold one code byte per element and one fp32
+ * scale per (token, KV head), separately for K and V; the value is
+ * code * scale.  fp8 codes are e4m3 (the OCP 8-bit floating point E4M3
+ * encoding without infinities, largest finite magnitude 448). */
+typedef enum { FA_KV_BF16 = 0, FA_KV_INT8 = 1, FA_KV_FP8 = 2 } fa_kv_dtype;
 typedef enum { FA_FULL = 0, FA_SLIDING = 1 } fa_layer_kind;
 
 /* kv_source values besides an explicit earlier layer index */
@@ -164,7 +172,7 @@ FA_API fa_status fa_cache_slab_bytes(const fa_cache* cache, int32_t layer, size_
                               size_t* scale_bytes);
 
 /* Bind caller-owned device buffers as the slab of an owning layer (k, v in the
- * layout above; k_scale, v_scale required in the int8 format, ignored in
+ * layout above; k_scale, v_scale required in the 8-bit formats, ignored in
  * bf16).  Binding a shared layer returns FA_ERR_INVALID_ARG: it reads its
  * source's slab.  Rebinding replaces the previous pointers.  Encodes the TMA
  * descriptors the kernels use, so it needs a CUDA device (FA_ERR_CUDA when the
@@ -189,6 +197,9 @@ FA_API size_t fa_kv_bytes_per_token(const fa_cache* cache, int32_t kind);
  * bf16 format: a bit-exact copy.  int8 format: per (token, head), separately
  * for K and V, a = max|x| in fp32, s = a / 127 (IEEE division), codes
  * c = clamp(rint(x / s), -127, 127) with rint rounding half to even; a = 0
+ * gives s = 0 and all-zero codes.  fp8 format: the same with s = a / 448
+ * and codes the e4m3 value nearest to the fp32 quotient x / s (ties to the
+ * even mantissa, magnitudes above 448 saturating to 448, sign kept); a = 0
  * gives s = 0 and all-zero codes.
  * A KV-shared layer stores nothing: FA_OK, no launch.  T == 0: FA_OK, no
  * launch. */
@@ -241,7 +252,7 @@ FA_API fa_status fa_paged_decode_attn(fa_cache* cache, int32_t layer, const void
  * position seq_lens[b] - 1 (negative: not stored; past the pool: not stored,
  * FA_DEV_ERR_SLOT).  The slot must be the one the block table gives for that
  * position, as with the two separate calls.  Rows are stored in the slab's
- * format (bf16 copy, or the int8 quantisation of fa_kv_store, bit for bit)
+ * format (bf16 copy, or the 8-bit quantisation of fa_kv_store, bit for bit)
  * by the CTA that reads the tile holding that position, before it reads it;
  * sequences with seq_lens[b] <= 0 still get their row stored.  For a shared
  * layer k_new, v_new and slot_mapping are ignored (may be NULL) and the call
@@ -328,9 +339,9 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * k_extend / v_extend; "pegainfer issue #807": the prefill chunk size is a
  * capacity parameter).  Sequence b has prefix_lens[b] = P_b tokens already
  * in the cache and n_b = qo_indptr[b+1] - qo_indptr[b] new tokens; new token
- * i sits at position P_b + i and attends to prefix positions (from the slab,
- * dequantised in int8) and chunk positions P_b + j, j <= i (from k_ext /
- * v_ext, bf16, never quantised), under the layer's mask.
+ * i sits at position P_b + i and attends to prefix positions (from the slab)
+ * and chunk positions P_b + j, j <= i (from k_ext / v_ext, bf16, never
+ * quantised), under the layer's mask.
  * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
  * (for a shared layer: the source layer's current k, v).  qo_indptr: int32
  * [B+1], non-decreasing, qo_indptr[0] = 0.  num_tokens: the rows of q, k_ext,
@@ -363,7 +374,7 @@ FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void
  * lengths including the new tokens, <= max_seq_len; a length below n_b sets
  * FA_DEV_ERR_BOUND), block_table: int32 [B][max_pages_per_seq].  out: bf16
  * [num_tokens][Hq][D]; lse: optional float [num_tokens][Hq].  bf16 slabs
- * only (int8: FA_ERR_UNSUPPORTED); Hq / Hkv must divide 128. */
+ * only (int8, fp8: FA_ERR_UNSUPPORTED); Hq / Hkv must divide 128. */
 FA_API fa_status fa_paged_decode_multi_attn(fa_cache* cache, int32_t layer, const void* q, const int32_t* qo_indptr,
                                             const int32_t* seq_lens, const int32_t* block_table,
                                             int32_t max_pages_per_seq, int32_t B, int32_t num_tokens,

@@ -102,10 +102,11 @@ class DecodeCase:
             if self.poison:
                 self._poison(i, d)
             return
-        # int8: quantise seeded bf16 context rows through the library's store
+        # 8-bit: quantise seeded bf16 context rows through the library's store;
+        # slots it does not write keep junk codes (e4m3: the NaN codes)
         nan = torch.tensor(float("nan"))
-        k_s.fill_(77)
-        v_s.fill_(-77)
+        k_s.fill_(0x7F if self.kv_dtype == W.KV_FP8 else 77)
+        v_s.fill_(0xFF if self.kv_dtype == W.KV_FP8 else -77)
         ks_s.fill_(nan)
         vs_s.fill_(nan)
         rows, slots = [], []
@@ -208,7 +209,8 @@ class DecodeCase:
             slabs = {o: (sk, sv)}
         else:
             H, D = owner_d["num_kv_heads"], owner_d["head_dim"]
-            ck = np.zeros((len(phys), H, self.ps, D), np.int8)
+            store_q = oracle.store_fp8 if self.kv_dtype == W.KV_FP8 else oracle.store_int8
+            ck = np.zeros((len(phys), H, self.ps, D), np.uint8 if self.kv_dtype == W.KV_FP8 else np.int8)
             cv = np.zeros_like(ck)
             sk = np.zeros((len(phys), H, self.ps), np.float32)
             sv = np.zeros_like(sk)
@@ -227,11 +229,11 @@ class DecodeCase:
                 kr = bits(k_rows[st:st + (hi - lo)])[sel]
                 vr = bits(v_rows[st:st + (hi - lo)])[sel]
                 sl = W.slots_for_positions(bt_c[n], pos[sel], self.ps)
-                oracle.store_int8(ck, cv, sk, sv, kr, vr, sl, self.ps)
+                store_q(ck, cv, sk, sv, kr, vr, sl, self.ps)
             k_new, v_new = self.new_kv[o]
             slots = [bt_c[n, (int(self.lens[b]) - 1) // self.ps] * self.ps + (int(self.lens[b]) - 1) % self.ps
                      for n, b in enumerate(seqs)]
-            oracle.store_int8(ck, cv, sk, sv, bits(k_new[seqs]), bits(v_new[seqs]), slots, self.ps)
+            store_q(ck, cv, sk, sv, bits(k_new[seqs]), bits(v_new[seqs]), slots, self.ps)
             slabs = {o: (ck, cv, sk, sv)}
         q = bits(self.q[i][seqs])
         sub_layers = [dict(l) for l in self.layers]

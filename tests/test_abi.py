@@ -62,7 +62,7 @@ def e_series(n_layers, period, n_owning, hkv, share=True):
 def test_sources_and_bytes_match_oracle(fa, model):
     for share in (True, False):
         layers = e_series(*model, share=share)
-        for dtype in (fa.KV_BF16, fa.KV_INT8):
+        for dtype in (fa.KV_BF16, fa.KV_INT8, fa.KV_FP8):
             c = fa.Cache(layers, 64, 16, dtype)
             want = oracle.resolve_kv_sources(layers)
             got = [c.source(i) for i in range(len(layers))]
@@ -72,9 +72,9 @@ def test_sources_and_bytes_match_oracle(fa, model):
             for i in range(len(layers)):
                 kv, sc = c.slab_bytes(i)
                 if want[i] == -1:
-                    elem = 1 if dtype == fa.KV_INT8 else 2
+                    elem = 2 if dtype == fa.KV_BF16 else 1
                     assert kv == 64 * layers[i]["num_kv_heads"] * 16 * layers[i]["head_dim"] * elem
-                    assert sc == (64 * layers[i]["num_kv_heads"] * 16 * 4 if dtype == fa.KV_INT8 else 0)
+                    assert sc == (0 if dtype == fa.KV_BF16 else 64 * layers[i]["num_kv_heads"] * 16 * 4)
                 else:
                     assert (kv, sc) == (0, 0)
 
@@ -85,9 +85,10 @@ def test_bytes_per_token_golden(fa):
             if l.strip() and not l.startswith("#")]
     models = {"E2B": (35, 5, 15, 1), "E4B": (42, 6, 24, 2)}
     for model, f, sharing, full, window in rows:
-        c = fa.Cache(e_series(*models[model], share=sharing == "after"), 8, 16,
-                     fa.KV_INT8 if f == "int8" else fa.KV_BF16)
-        assert (c.bytes_per_token(FULL), c.bytes_per_token(SLIDING)) == (int(full), int(window))
+        # the page's 8-bit figures hold for the int8 and the fp8 format alike
+        for dtype in ((fa.KV_INT8, fa.KV_FP8) if f == "int8" else (fa.KV_BF16,)):
+            c = fa.Cache(e_series(*models[model], share=sharing == "after"), 8, 16, dtype)
+            assert (c.bytes_per_token(FULL), c.bytes_per_token(SLIDING)) == (int(full), int(window))
 
 
 def test_refusals(fa):

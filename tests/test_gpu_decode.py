@@ -49,7 +49,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8, W.KV_FP8], ids=["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("spec", SMALL, ids=[f"{'F' if s[0] == 0 else 'S'}{s[1]}_g{s[2] // s[3]}_W{s[4]}"
                                              for s in SMALL])
 def test_small_decode(spec, kv_dtype):
@@ -116,7 +116,7 @@ def test_determinism_and_graph_replay():
         assert torch.equal(a, b) and torch.equal(la, lb)
 
 
-@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8, W.KV_FP8], ids=["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("shape", ["d256_g8", "d256_g8_one_kv", "d512_g8"])
 def test_repeated_decodes_are_bit_identical(shape, kv_dtype):
     """Alternating layers with many short segments per CTA (one-tile and
@@ -175,8 +175,9 @@ def test_long_context_decode_full_size():
     check_layers(case, _sample(case.B, 3, 3), layers=[0, 4, 7, 9])
 
 
-def test_int8_decode_full_size():
-    w = W.int8_decode()
+@pytest.mark.parametrize("make", [W.int8_decode, W.fp8_decode], ids=["int8", "fp8"])
+def test_8bit_decode_full_size(make):
+    w = make()
     case = DecodeCase(w.layers, W.seq_lens(w), w.page_size, w.kv_dtype, w.seed)
     lens = case.lens
     seqs = sorted(set(_sample(case.B, 4, 5) + [int(np.argmax(lens))]))
@@ -217,7 +218,7 @@ def test_early_metadata_flag_gives_identical_results():
     assert case.fa.device_error() == 0
 
 
-@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8, W.KV_FP8], ids=["bf16", "int8", "fp8"])
 def test_window_pool(kv_dtype):
     """Sliding layers on a pool of their own: their tables hold only the
     in-window pages (-1 elsewhere) and index a pool sized for the windows,

@@ -40,7 +40,7 @@ def _decode_groups(case, lse=True):
     return outs, lses
 
 
-@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8, W.KV_FP8], ids=["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("lens", [[3, 33, 34, 49, 150, 700, 1, 517], [600] * 12 + [2049, 16, 17]],
                          ids=["mixed", "uniform"])
 def test_layers_decode_equals_per_layer(kv_dtype, lens):
@@ -74,7 +74,7 @@ def test_layers_decode_matches_oracle_on_the_tiny_workload():
     assert case.fa.device_error() == 0
 
 
-@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8, W.KV_FP8], ids=["bf16", "int8", "fp8"])
 def test_store_layers_equals_per_layer_stores(kv_dtype):
     import full_attention_gb300 as fa
     layers = W.layout_12(8, 1, 64)

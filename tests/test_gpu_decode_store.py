@@ -43,7 +43,7 @@ def run_both(layers, lens, kv_dtype, seed, flags=0):
     return sep, fus, res_sep, res_fus
 
 
-@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", [W.KV_BF16, W.KV_INT8, W.KV_FP8], ids=["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("ci", range(len(CASES)))
 def test_fused_equals_store_then_decode(ci, kv_dtype):
     layers, lens = CASES[ci]

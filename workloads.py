@@ -30,6 +30,7 @@ KV_AUTO = -2  # shared layer: source = last earlier owning layer of its kind
 
 KV_BF16 = 0
 KV_INT8 = 1
+KV_FP8 = 2
 
 
 def layer(kind: int, head_dim: int, hq: int, hkv: int, window: int = 0,
@@ -117,9 +118,16 @@ def int8_decode() -> DecodeWorkload:
                           layout_12(8, 1, 1024), kv_dtype=KV_INT8)
 
 
+def fp8_decode() -> DecodeWorkload:
+    """The int8 decode workload's shapes with the fp8 e4m3 per-token-head format."""
+    return DecodeWorkload("fp8 e4m3 per-token-head KV decode (B=128, ctx U[1024,8192], 8q/1kv, "
+                          "S D256 W1024 / F D512)", 4, 128, 1024, 8192, 16,
+                          layout_12(8, 1, 1024), kv_dtype=KV_FP8)
+
+
 ALL = {"tiny_decode": tiny_decode, "e2b_decode": e2b_decode,
        "chunked_prefill": chunked_prefill, "long_decode": long_decode,
-       "int8_decode": int8_decode}
+       "int8_decode": int8_decode, "fp8_decode": fp8_decode}
 
 
 # ---------------------------------------------------------------------------
