@@ -66,6 +66,9 @@ struct ExtCfg {
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
+  // 16-row groups 0 .. TMA_GROUPS - 1 of a prefix tile come by TMA, the
+  // others by the producer warp's cp.async copies (two copy paths in parallel)
+  static constexpr int TMA_GROUPS = 4;
   static constexpr int NPW = 4;                 // producer warps
   static constexpr int W_MMA = NPW;             // the MMA warp; the softmax warps follow it
   static constexpr int NSMX = 8;                // softmax warps: two per tensor-memory lane quarter
@@ -294,6 +297,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       for (int g = 0; g < 4; ++g) ts.row0[g] = __shfl_sync(0xffffffffu, r0, g);
       return ts;
     };
+    // group g of a prefix tile goes by TMA: a whole page group of readable keys
+    auto by_tma = [&](const TileSrc& ts, int g) {
+      return g < C::TMA_GROUPS && g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
+    };
     int e = 0;
     bool ok = true;
     // one slot: column blocks blk0 .. blk0 + CPS - 1 (8 KB each)
@@ -310,13 +317,13 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
               int tx = 0;
 #pragma unroll
               for (int g = 0; g < 4; ++g)
-                if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim) tx += C::CPS * 2048;
+                if (by_tma(ts, g)) tx += C::CPS * 2048;
               mbar_arrive_expect_tx(&full[sl], tx);
 #pragma unroll
               for (int h = 0; h < C::CPS; ++h)
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                  if (g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim)
+                  if (by_tma(ts, g))
                     tma_load_3d(dst + h * C::CHUNK + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk0 + h,
                                 ts.row0[g], pol);
             }
@@ -328,8 +335,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
             bool any_cp = false;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              const bool tma = g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
-              if (tma) continue;
+              if (by_tma(ts, g)) continue;
               any_cp = true;
               // 16 rows x 8 units per block: lane copies rows lane / 8 + 4 i, unit lane % 8
 #pragma unroll
