@@ -83,6 +83,11 @@ struct ExtCfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 1) * 8 <= BAR_BYTES, "barrier space");
   static_assert(NSLOT >= KB / CPS + NVB / CPS, "a ring must hold one tile");
+  // a producer warp's consecutive slots lie NPW ring positions apart; its
+  // parity wait on a slot's empty barrier is sound only while that is at most
+  // one lap of the ring (else the barrier may be two phases behind and the
+  // parity of an older phase passes the wait early)
+  static_assert(NPW <= NSLOT, "producer stride within one ring lap");
   static_assert(KB % CPS == 0 && NVB % CPS == 0, "slots hold whole groups of column blocks");
 };
 
