@@ -68,7 +68,7 @@ struct ExtCfg {
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   // 16-row groups 0 .. TMA_GROUPS - 1 of a prefix tile come by TMA, the
   // others by the producer warp's cp.async copies (two copy paths in parallel)
-  static constexpr int TMA_GROUPS = 4;
+  static constexpr int TMA_GROUPS = 2;
   static constexpr int NPW = 4;                 // producer warps
   static constexpr int W_MMA = NPW;             // the MMA warp; the softmax warps follow it
   static constexpr int NSMX = 8;                // softmax warps: two per tensor-memory lane quarter
