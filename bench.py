@@ -272,6 +272,19 @@ class DecodeStep:
                 events[i][1].record()
 
 
+def reduce_over_ranks(value: float, op: str, world: int, device="cpu") -> float:
+    """max or sum of one float over the ranks of the process group (every rank
+    gets the result); the value itself when running alone.  Replicas are
+    independent: this is the only cross-rank exchange, outside the timed
+    region."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX if op == "max" else torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
 def gpu_arm(args, rank, world):
     import torch
     import full_attention_gb300 as fa
@@ -344,10 +357,11 @@ def gpu_arm(args, rank, world):
         torch.distributed.barrier()
     assert fa.device_error() == 0
     t_step = sum(step_ms) / len(step_ms) / 1e3       # seconds per step (device time)
-    t_tot = torch.tensor([sum(step_ms)], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_tot, op=torch.distributed.ReduceOp.MAX)
-    t_max = float(t_tot.item()) / 1e3 / args.steps
+    # the slowest rank's time; the bytes every rank's replica moved (replicas
+    # are seeded per rank, so their lengths differ)
+    t_max = reduce_over_ranks(sum(step_ms), "max", world, dev) / 1e3 / args.steps
+    job_bytes = reduce_over_ranks(step.step_bytes, "sum", world, dev)
+    job_unique = reduce_over_ranks(step.unique_bytes, "sum", world, dev)
     hbm, bf16, bf16s, peak_src = measured_peaks()
     dec_bytes = sum(step.decode_bytes)
     dec_time = sum(dec_ms) / 1e3 / n_ev               # seconds of decode launches per step
@@ -368,7 +382,7 @@ def gpu_arm(args, rank, world):
     clocks = clk.summary()
     res = {
         "metric": "paged decode-attn achieved HBM GB/s (% of peak); chunked-prefill TFLOP/s",
-        "value": round(step.step_bytes * world / t_max / 1e9, 1),
+        "value": round(job_bytes / t_max / 1e9, 1),
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_max * 1e3, 4),
@@ -380,9 +394,9 @@ def gpu_arm(args, rank, world):
                    "graph": graph is not None, "early_metadata": True,
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(step.B * world / t_max, 1),
-        "pct_of_peak": round(100 * step.step_bytes / t_max / 1e9 / hbm, 1),
+        "pct_of_peak": round(100 * job_bytes / world / t_max / 1e9 / hbm, 1),
         "unique_bytes_per_step": int(step.unique_bytes),
-        "unique_gb_per_s": round(step.unique_bytes * world / t_max / 1e9, 1),
+        "unique_gb_per_s": round(job_unique / t_max / 1e9, 1),
         "roofline": {"kernel": "decode_kernel (paged decode attention, split-K merged in-kernel)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_source": peak_src,
@@ -395,8 +409,17 @@ def gpu_arm(args, rank, world):
         "wall_s_timed": round(wall, 3),
     }
     res["multi_layer_step"] = multi_layer_measure(step, args, torch, flush, hbm)
+    # end to end on every rank; the job's bytes over the slowest rank's time
+    if world > 1:
+        torch.distributed.barrier()
+    e2 = e2e_decode(step, args, torch)
+    t_e2e = reduce_over_ranks(e2["ms_per_step"], "max", world, dev) / 1e3
+    e2["value"] = round(job_bytes / t_e2e / 1e9, 1)
+    e2["ms_per_step"] = round(t_e2e * 1e3, 4)
+    e2["h2d_bytes_per_step"] = int(reduce_over_ranks(e2["h2d_bytes_per_step"], "sum", world, dev))
+    e2["d2h_bytes_per_step"] = int(reduce_over_ranks(e2["d2h_bytes_per_step"], "sum", world, dev))
+    res["e2e"] = e2
     if rank == 0:
-        res["e2e"] = e2e_decode(step, args, torch)
         if args.workload == "e2b_decode" and not args.no_prefill:
             res["prefill"] = prefill_measure(args, dev)
         if not args.no_cpu_baseline:
@@ -539,7 +562,7 @@ def e2e_decode(step, args, torch):
         assert torch.equal(g, t.contiguous().view(torch.uint8).view(-1).cpu()), "end-to-end output differs"
     t = tot / n / 1e3
     return {"value": round(step.step_bytes / t / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "ms_per_step": round(t * 1e3, 4),
+            "d2h_bytes_per_step": bo, "ms_per_step": t * 1e3,
             "path": "C-ABI calls; one host-to-device and one device-to-host copy per step (pinned buffers)"}
 
 
