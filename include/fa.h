@@ -73,7 +73,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer ... */
-  FA_ERR_UNSUPPORTED = 2,   /* a layout the method refuses or this build lacks */
+  FA_ERR_UNSUPPORTED = 2,   /* a layout the method refuses or the library does not implement */
   FA_ERR_NOT_BOUND = 3,     /* the layer's slab owner has no slab bound yet   */
   FA_ERR_WORKSPACE = 4,     /* workspace smaller than fa_decode_workspace_bytes */
   FA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed           */
