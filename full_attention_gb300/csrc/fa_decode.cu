@@ -49,7 +49,10 @@ struct DecCfg {
   static constexpr int ROWB = D * ELEM;                 // bytes per row
   static constexpr int NBLK = ROWB / 128;               // 128-byte column blocks per row
   static constexpr int TILE_BYTES = kTile * ROWB;       // one 16-row tile of K (or V)
-  static constexpr int NT = 32768 / (2 * TILE_BYTES);   // tiles per pipeline step (32 KB of K+V)
+  // tiles per pipeline step: 32 KB of K+V, but at most 2, since more tiles
+  // per step lengthen the consumer chain between barriers (8-bit head_dim
+  // 256 measured 2% faster at 2 tiles than at 4, slower at 1)
+  static constexpr int NT = 32768 / (2 * TILE_BYTES) < 2 ? 32768 / (2 * TILE_BYTES) : 2;
   static constexpr int NSTAGE = 3;
   static constexpr int PREFETCH_TILES = 2 * NSTAGE * NT; // tiles a CTA pulls into L2 before its dependency resolves
   static constexpr int NCW = 4;                         // consumer warps
