@@ -669,8 +669,6 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   const int g = L.d.num_q_heads / L.d.num_kv_heads;
   if (128 % g != 0)
     return fail(FA_ERR_UNSUPPORTED, "extend packs Hq/Hkv = %d query heads into 128-row tiles; it must divide 128", g);
-  if (c->kv_dtype != FA_KV_BF16)
-    return fail(FA_ERR_UNSUPPORTED, "extend over the 8-bit per-token-head formats is not built");
   const Slab* s = nullptr;
   if ((st = check_bound(c, layer, &s))) return st;
   if (!q || !k_ext || !v_ext || !qo_indptr || !prefix_lens || !out || (max_prefix_len > 0 && !block_table))
@@ -736,8 +734,6 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   const int g = L.d.num_q_heads / L.d.num_kv_heads;
   if (128 % g != 0)
     return fail(FA_ERR_UNSUPPORTED, "multi-token decode packs Hq/Hkv = %d query heads into 128-row tiles; it must divide 128", g);
-  if (c->kv_dtype != FA_KV_BF16)
-    return fail(FA_ERR_UNSUPPORTED, "multi-token decode over the 8-bit per-token-head formats is not built");
   const Slab* s = nullptr;
   if ((st = check_bound(c, layer, &s))) return st;
   if (!q || !qo_indptr || !seq_lens || !block_table || !out) return fail(FA_ERR_INVALID_ARG, "a required pointer is NULL");

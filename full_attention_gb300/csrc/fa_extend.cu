@@ -32,8 +32,13 @@
 //               S buffer; rescale O in TMEM only when the running max grows by
 //               more than 2^8, so rescales are rare; final normalisation and
 //               bf16 store.
+// 8-bit slabs (int8 or fp8 per-token-head codes): the producers dequantise
+// the prefix rows (code * scale, rounded to bf16) into the same shared-memory
+// layout instead of copying them; the chunk rows are bf16 either way.
 // Every wait is bounded; tensor memory is always freed.
 #include <cfloat>
+
+#include <cuda_fp8.h>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -93,8 +98,10 @@ struct ExtCfg {
 
 struct ExtK {
   const __nv_bfloat16* q;
-  const uint8_t* k_slab;   // [rows][D] bf16, rows = (page * Hkv + head) * page_size + offset
+  const uint8_t* k_slab;   // [rows][D] bf16 (or 8-bit codes), rows = (page * Hkv + head) * page_size + offset
   const uint8_t* v_slab;
+  const float* k_scale;    // 8-bit slabs: [rows] fp32 scales
+  const float* v_scale;
   const uint8_t* k_ext;    // [num_tokens][Hkv][D] bf16
   const uint8_t* v_ext;
   const int32_t* qo_indptr;
@@ -174,7 +181,56 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   return true;
 }
 
-template <int D>
+// f16 pair of two fp32 values, magnitudes above the f16 range saturating.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  return pack_f16x2(fminf(fmaxf(lo, -65504.f), 65504.f), fminf(fmaxf(hi, -65504.f), 65504.f));
+}
+
+// 32 consecutive 8-bit codes (two 16-byte words) times the row's scale,
+// rounded once and packed in pairs: bf16 for K (the S MMA's operand, Q being
+// bf16), f16 for V (the PV MMA runs in f16 for 8-bit slabs, P being f16, so
+// the dequantised V keeps three more mantissa bits).  int8 codes are exact in
+// fp32, e4m3 codes exact in f16.
+template <int KV, bool F16>
+__device__ __forceinline__ void dequant32(const uint4 (&w)[2], float s, uint32_t (&out)[16]) {
+  const uint32_t word[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float f[4];
+    if constexpr (KV == FA_KV_INT8) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) f[b] = static_cast<float>(static_cast<int8_t>((word[i] >> (8 * b)) & 0xffu));
+    } else {
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(word[i] >> (16 * b)), __NV_E4M3);
+        __half2 hh;
+        hh.x = __ushort_as_half(hr.x);
+        hh.y = __ushort_as_half(hr.y);
+        const float2 ff = __half22float2(hh);
+        f[2 * b] = ff.x;
+        f[2 * b + 1] = ff.y;
+      }
+    }
+    if constexpr (F16) {
+      out[2 * i] = pack_f16x2_sat(f[0] * s, f[1] * s);
+      out[2 * i + 1] = pack_f16x2_sat(f[2] * s, f[3] * s);
+    } else {
+      out[2 * i] = pack_bf16x2(f[0] * s, f[1] * s);
+      out[2 * i + 1] = pack_bf16x2(f[2] * s, f[3] * s);
+    }
+  }
+}
+
+// 32 consecutive bf16 values (four 16-byte words) as f16 pairs (saturating).
+__device__ __forceinline__ void bf16_to_f16_32(const uint4 (&w)[4], uint32_t (&out)[16]) {
+  const uint32_t word[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
+                             w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) out[i] = pack_f16x2_sat(__uint_as_float(word[i] << 16), __uint_as_float(word[i] & 0xffff0000u));
+}
+
+template <int D, int KV>
 __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kx,
@@ -241,10 +297,14 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     const int pw = warp;
     const uint64_t pol = l2_policy_evict_last();   // K/V rows are shared by the CTAs of a (sequence, head)
     if (threadIdx.x == 0) {
-      prefetch_tmap(&tm_q);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int kb = C::NQT; kb < C::KB; ++kb)
-        tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
+      if constexpr (KV == FA_KV_BF16) {
+        prefetch_tmap(&tm_q);
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+        for (int kb = C::NQT; kb < C::KB; ++kb)
+          tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
+      } else {
+        mbar_arrive_expect_tx(q_full, 0);   // the softmax warps write Q, as f16, themselves
+      }
     }
     if (lane == 0) {
       prefetch_tmap(&tm_k);
@@ -317,7 +377,74 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         ok = __shfl_sync(0xffffffffu, w, 0) && ok;
         if (ok) {
           uint8_t* dst = ring + sl * C::SLOT;
-          if (ts.prefix) {
+          if constexpr (KV != FA_KV_BF16) {
+            if (ts.prefix) {
+              // 8-bit slab: lane (row rr, half cpart) dequantises 32 codes of
+              // one row per (group, column block) into the bf16 layout the TMA
+              // boxes would give; rows that hold no visible key read as zero
+              const uint8_t* codes = is_v ? p.v_slab : p.k_slab;
+              const float* scl = is_v ? p.v_scale : p.k_scale;
+              const int rr = lane >> 1, cpart = lane & 1;
+              float s4[4];
+              bool v4[4];
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int r = 16 * g + rr;
+                v4[g] = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
+                s4[g] = v4[g] ? __ldg(scl + (v4[g] ? ts.row0[g] + rr : 0)) : 0.f;
+              }
+#pragma unroll 1
+              for (int h = 0; h < C::CPS; ++h) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const uint4* src = reinterpret_cast<const uint4*>(
+                      codes + static_cast<size_t>(v4[g] ? ts.row0[g] + rr : 0) * D + (blk0 + h) * 64 + cpart * 32);
+                  uint4 w[2];
+                  w[0] = v4[g] ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
+                  w[1] = v4[g] ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+                  uint32_t pk[16];
+                  dequant32<KV, true>(w, s4[g], pk);
+#pragma unroll
+                  for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(16 * g + rr, cpart * 4 + u)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+              }
+              // the generic writes, ordered for the MMA's async-proxy reads;
+              // full[] counts lane 0's (empty) expect_tx and 32 lane arrivals
+              fence_proxy_async_smem();
+              if (lane == 0) mbar_arrive_expect_tx(&full[sl], 0);
+              mbar_arrive(&full[sl]);
+            } else {
+              // chunk K and V rows (bf16) as f16 for the MMAs; rows past the
+              // chunk read as zero
+              const uint8_t* ext = is_v ? p.v_ext : p.k_ext;
+              const int rr = lane >> 1, cpart = lane & 1;
+#pragma unroll 1
+              for (int h = 0; h < C::CPS; ++h) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const int r = 16 * g + rr;
+                  const bool v = r < ts.lim;
+                  const uint4* src = reinterpret_cast<const uint4*>(
+                      ext + ((static_cast<size_t>(v ? ts.tok0 + r : 0) * p.Hkv + x.h) * D + (blk0 + h) * 64 +
+                             cpart * 32) * 2);
+                  uint4 w[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) w[i] = v ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+                  uint32_t pk[16];
+                  bf16_to_f16_32(w, pk);
+#pragma unroll
+                  for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(r, cpart * 4 + u)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+              }
+              fence_proxy_async_smem();
+              if (lane == 0) mbar_arrive_expect_tx(&full[sl], 0);
+              mbar_arrive(&full[sl]);
+            }
+          } else if (ts.prefix) {
             if (lane == 0) {
               int tx = 0;
 #pragma unroll
@@ -394,8 +521,12 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     // The whole warp walks the schedule and waits on the barriers, so slot
     // addresses and descriptors are warp-uniform; one elected lane (always
     // the same one) issues the MMAs and the commits that track them.
-    const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);
-    const uint32_t idO = umma_idesc_bf16(C::M, 64 * C::CPS, true);   // the V blocks of a slot, LBO = CHUNK
+    // 8-bit slabs: Q, K, P and V are all f16 (dequantised values keep 11
+    // significant bits); bf16 slabs: all bf16, as stored
+    const uint32_t idS = KV == FA_KV_BF16 ? umma_idesc_bf16(C::M, C::NK, false) : umma_idesc_f16(C::M, C::NK, false);
+    // the V blocks of a slot, LBO = CHUNK; P and V are f16 for 8-bit slabs
+    const uint32_t idO = KV == FA_KV_BF16 ? umma_idesc_bf16(C::M, 64 * C::CPS, true)
+                                          : umma_idesc_f16(C::M, 64 * C::CPS, true);
     bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0) && mbar_wait(qt_full, 0));
     tc_fence_after();
     const uint64_t qd0 = umma_desc_sw128(smem_u32(qs), 16, 1024);   // Q's shared-memory blocks
@@ -499,12 +630,16 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     {
       // this row's first NQT * 64 query values into tensor memory (row =
       // lane, bf16 pairs per column: the A-operand layout of the S MMA),
-      // half h copying blocks h, h + 2, ...; rows past the last token are zero
+      // half h copying blocks h, h + 2, ...; rows past the last token are zero.
+      // For 8-bit slabs the MMAs run in f16: every block of the row goes as
+      // f16, the rest of Q into its shared-memory blocks (the layout the TMA
+      // boxes would give)
       const int tok = x.qo0 + t;
       const bool in = tok < p.num_tokens;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
+      constexpr int QBLK = KV == FA_KV_BF16 ? C::NQT : C::KB;
 #pragma unroll 1
-      for (int kb = half; kb < C::NQT; kb += 2) {
+      for (int kb = half; kb < QBLK; kb += 2) {
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -514,8 +649,20 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
           w[4 * i + 2] = v.z;
           w[4 * i + 3] = v.w;
         }
-        tmem_st32(trow + C::Q_COL0 + kb * 32, w);
+        if constexpr (KV != FA_KV_BF16) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = pack_f16x2_sat(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        }
+        if (kb < C::NQT) {
+          tmem_st32(trow + C::Q_COL0 + kb * 32, w);
+        } else {
+          uint8_t* qb = qs + (kb - C::NQT) * (C::M * 128);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(qb + sw128(r, u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
       }
+      if constexpr (KV != FA_KV_BF16) fence_proxy_async_smem();   // the Q rows written here, for the S MMA
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -597,9 +744,16 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       for (int c = 0; c < 16; ++c) {
         const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
         const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
-        pk[c] = pack_bf16x2(p0, p1);
-        // the denominator sums the bf16-rounded weights the PV MMA uses
-        ps[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+        // the denominator sums the rounded weights the PV MMA uses (bf16, or
+        // f16 for 8-bit slabs)
+        if constexpr (KV == FA_KV_BF16) {
+          pk[c] = pack_bf16x2(p0, p1);
+          ps[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+        } else {
+          pk[c] = pack_f16x2(p0, p1);
+          const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pk[c]));
+          ps[c & 3] += pf.x + pf.y;
+        }
       }
       l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       tmem_st16(trow + s_col + 16 * half, pk);   // P of keys [32 half, 32 half + 32): 16 columns of bf16 pairs
@@ -653,14 +807,14 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   }
 }
 
-template <int D>
+template <int D, int KV>
 static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStream_t s) {
   using C = ExtCfg<D>;
   static unsigned int done = 0;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend_kernel<D>), C::SMEM_ALLOC, &done);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend_kernel<D, KV>), C::SMEM_ALLOC, &done);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
-  return launch_pdl(extend_kernel<D>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
+  return launch_pdl(extend_kernel<D, KV>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
                     a.tm_vx, k);
 }
 
@@ -669,6 +823,8 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
   k.q = static_cast<const __nv_bfloat16*>(a.q);
   k.k_slab = static_cast<const uint8_t*>(a.k_slab);
   k.v_slab = static_cast<const uint8_t*>(a.v_slab);
+  k.k_scale = a.k_scale;
+  k.v_scale = a.v_scale;
   k.k_ext = static_cast<const uint8_t*>(a.k_ext);
   k.v_ext = static_cast<const uint8_t*>(a.v_ext);
   k.num_tokens = a.num_tokens;
@@ -696,8 +852,11 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
   k.dslices = a.D / ExtCfg<256>::DS;
   k.early_metadata = a.early_metadata;
   k.scale_log2 = a.sm_scale * 1.4426950408889634f;
-  if (a.D == 256) return launch_extend_t<256>(a, k, s);
-  return launch_extend_t<512>(a, k, s);
+  if (a.kv_dtype == FA_KV_INT8)
+    return a.D == 256 ? launch_extend_t<256, FA_KV_INT8>(a, k, s) : launch_extend_t<512, FA_KV_INT8>(a, k, s);
+  if (a.kv_dtype == FA_KV_FP8)
+    return a.D == 256 ? launch_extend_t<256, FA_KV_FP8>(a, k, s) : launch_extend_t<512, FA_KV_FP8>(a, k, s);
+  return a.D == 256 ? launch_extend_t<256, FA_KV_BF16>(a, k, s) : launch_extend_t<512, FA_KV_BF16>(a, k, s);
 }
 
 }  // namespace fa

@@ -339,8 +339,9 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * k_extend / v_extend; "pegainfer issue #807": the prefill chunk size is a
  * capacity parameter).  Sequence b has prefix_lens[b] = P_b tokens already
  * in the cache and n_b = qo_indptr[b+1] - qo_indptr[b] new tokens; new token
- * i sits at position P_b + i and attends to prefix positions (from the slab)
- * and chunk positions P_b + j, j <= i (from k_ext / v_ext, bf16, never
+ * i sits at position P_b + i and attends to prefix positions (from the slab;
+ * in the 8-bit formats dequantised as code * scale, rounded to bf16) and
+ * chunk positions P_b + j, j <= i (from k_ext / v_ext, bf16, never
  * quantised), under the layer's mask.
  * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
  * (for a shared layer: the source layer's current k, v).  qo_indptr: int32
@@ -351,8 +352,8 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * FA_DEV_ERR_BOUND and are cut).  out: bf16 [N][Hq][D]; lse: optional float
  * [N][Hq].  The chunk's own k, v are read from k_ext / v_ext even if they
  * were stored first.  Hq / Hkv must divide 128 (query heads of a KV head are
- * packed into 128-row tensor-core tiles) and the format must be bf16; other
- * cases return FA_ERR_UNSUPPORTED. */
+ * packed into 128-row tensor-core tiles); other cases return
+ * FA_ERR_UNSUPPORTED.  Every slab format is served. */
 FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void* q, const void* k_ext,
                                const void* v_ext, const int32_t* qo_indptr,
                                const int32_t* prefix_lens, const int32_t* block_table,
@@ -373,8 +374,8 @@ FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void
  * qo_indptr[b+1] - qo_indptr[b] <= max_q_len), seq_lens: int32 [B] (device;
  * lengths including the new tokens, <= max_seq_len; a length below n_b sets
  * FA_DEV_ERR_BOUND), block_table: int32 [B][max_pages_per_seq].  out: bf16
- * [num_tokens][Hq][D]; lse: optional float [num_tokens][Hq].  bf16 slabs
- * only (int8, fp8: FA_ERR_UNSUPPORTED); Hq / Hkv must divide 128. */
+ * [num_tokens][Hq][D]; lse: optional float [num_tokens][Hq].  Every slab
+ * format (8-bit keys dequantised as in extend); Hq / Hkv must divide 128. */
 FA_API fa_status fa_paged_decode_multi_attn(fa_cache* cache, int32_t layer, const void* q, const int32_t* qo_indptr,
                                             const int32_t* seq_lens, const int32_t* block_table,
                                             int32_t max_pages_per_seq, int32_t B, int32_t num_tokens,

@@ -151,13 +151,14 @@ def test_cache_flags(fa):
     assert e.value.status == fa.ERR_INVALID_ARG
 
 
-def test_8bit_formats_refused_by_extend_and_multi_token_decode(fa):
-    """Extend and multi-token decode serve bf16 slabs only; the 8-bit formats
-    are refused before any pointer is read or any launch is made."""
-    for dtype in (fa.KV_INT8, fa.KV_FP8):
+def test_8bit_formats_reach_extend_and_multi_token_decode(fa):
+    """Extend and multi-token decode serve the 8-bit formats: with no slab
+    bound the calls stop at that check (before any pointer is read or any
+    launch is made), not at a format refusal."""
+    for dtype in (fa.KV_BF16, fa.KV_INT8, fa.KV_FP8):
         c = fa.Cache([lay(FULL, 512, 8, 1)], 8, 16, dtype)
         st = fa.lib().fa_paged_extend_attn(c._h, 0, None, None, None, None, None, None, 1, 2, 4, 2, 16, None, None,
                                            None)
-        assert st == fa.ERR_UNSUPPORTED
+        assert st == fa.ERR_NOT_BOUND
         st = fa.lib().fa_paged_decode_multi_attn(c._h, 0, None, None, None, None, 1, 2, 4, 2, 16, None, None, None)
-        assert st == fa.ERR_UNSUPPORTED
+        assert st == fa.ERR_NOT_BOUND
