@@ -340,9 +340,11 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * capacity parameter).  Sequence b has prefix_lens[b] = P_b tokens already
  * in the cache and n_b = qo_indptr[b+1] - qo_indptr[b] new tokens; new token
  * i sits at position P_b + i and attends to prefix positions (from the slab;
- * in the 8-bit formats dequantised as code * scale, rounded to bf16) and
- * chunk positions P_b + j, j <= i (from k_ext / v_ext, bf16, never
- * quantised), under the layer's mask.
+ * in the 8-bit formats dequantised as code * scale) and chunk positions
+ * P_b + j, j <= i (from k_ext / v_ext, bf16, never quantised), under the
+ * layer's mask.  Over 8-bit slabs every tensor-core operand (q, the
+ * dequantised and the chunk k, v, and the softmax weights) is f16, with fp32
+ * accumulation; magnitudes past the f16 range (65504) saturate.
  * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
  * (for a shared layer: the source layer's current k, v).  qo_indptr: int32
  * [B+1], non-decreasing, qo_indptr[0] = 0.  num_tokens: the rows of q, k_ext,
