@@ -162,3 +162,30 @@ def test_8bit_formats_reach_extend_and_multi_token_decode(fa):
         assert st == fa.ERR_NOT_BOUND
         st = fa.lib().fa_paged_decode_multi_attn(c._h, 0, None, None, None, None, 1, 2, 4, 2, 16, None, None, None)
         assert st == fa.ERR_NOT_BOUND
+
+
+def test_window_pool_sizes_the_sliding_slabs(fa):
+    """Sliding layers' slabs take the window pool's page count, full layers keep
+    the cache's; a shared layer owns nothing; the per-token cost is unchanged;
+    0 restores the single pool; bad sizes are refused (no GPU needed)."""
+    layers = [lay(SLIDING, 256, 8, 2, 64), lay(FULL, 512, 8, 1), lay(SLIDING, 256, 8, 2, 64, KV_AUTO)]
+    for dtype in (fa.KV_BF16, fa.KV_INT8, fa.KV_FP8):
+        c = fa.Cache(layers, 1000, 16, dtype)
+        elem = 2 if dtype == fa.KV_BF16 else 1
+        per_token = (c.bytes_per_token(FULL), c.bytes_per_token(SLIDING))
+        c.set_window_pool(40)
+        kv, sc = c.slab_bytes(0)
+        assert kv == 40 * 2 * 16 * 256 * elem and sc == (0 if dtype == fa.KV_BF16 else 40 * 2 * 16 * 4)
+        assert c.slab_bytes(1)[0] == 1000 * 1 * 16 * 512 * elem
+        assert c.slab_bytes(2) == (0, 0)
+        assert (c.layer_pages(0), c.layer_pages(1), c.layer_pages(2)) == (40, 1000, 40)
+        assert (c.bytes_per_token(FULL), c.bytes_per_token(SLIDING)) == per_token
+        c.set_window_pool(0)
+        assert c.slab_bytes(0)[0] == 1000 * 2 * 16 * 256 * elem
+    c = fa.Cache(layers, 1000, 16)
+    with pytest.raises(fa.FAError) as e:
+        c.set_window_pool(-1)
+    assert e.value.status == fa.ERR_INVALID_ARG
+    with pytest.raises(fa.FAError) as e:
+        c.set_window_pool(1 << 27)   # 2^27 pages x 2 heads x 16 rows >= 2^31
+    assert e.value.status == fa.ERR_UNSUPPORTED
