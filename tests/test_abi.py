@@ -189,3 +189,37 @@ def test_window_pool_sizes_the_sliding_slabs(fa):
     with pytest.raises(fa.FAError) as e:
         c.set_window_pool(1 << 27)   # 2^27 pages x 2 heads x 16 rows >= 2^31
     assert e.value.status == fa.ERR_UNSUPPORTED
+
+
+def test_multi_layer_decode_argument_checks(fa):
+    """fa_paged_decode_attn_layers validates on the host, before any device
+    access: the layer count, duplicates, one head_dim per call, pointers,
+    alignment and the workspace size.  Host buffers stand in for device
+    pointers (never dereferenced by the checks)."""
+    import ctypes
+    layers = [lay(SLIDING, 256, 8, 1, 64), lay(SLIDING, 256, 8, 1, 64), lay(FULL, 512, 8, 1)]
+    c = fa.Cache(layers, 64, 16)
+    buf = np.zeros(1 << 16, np.uint8)
+    base = (buf.ctypes.data + 255) // 256 * 256          # a 256-byte aligned host address
+    lib = fa.lib()
+
+    def call(ids, B=2, maxlen=64, ws_bytes=1 << 20, q_off=0, ws_off=0, maxp=16):
+        n = len(ids)
+        ids_a = (ctypes.c_int32 * max(n, 1))(*ids)
+        ptr = (ctypes.c_void_p * max(n, 1))(*([base + q_off] * n))
+        lens = base + 4096
+        return lib.fa_paged_decode_attn_layers(c._h, n, ids_a, ptr, ptr, maxp, lens, B, maxlen, ptr, None,
+                                               base + 8192 + ws_off, ws_bytes, None)
+
+    assert call([]) == fa.ERR_INVALID_ARG                          # n < 1
+    assert call([0] * 17) == fa.ERR_INVALID_ARG                    # n > FA_MAX_LAYERS_PER_LAUNCH
+    assert call([0, 0]) == fa.ERR_INVALID_ARG                      # a layer twice
+    assert call([0, 2]) == fa.ERR_UNSUPPORTED                      # head_dims 256 and 512
+    assert call([0, 5]) == fa.ERR_INVALID_ARG                      # layer out of range
+    assert call([0, 1], q_off=8) == fa.ERR_INVALID_ARG             # q, out not 16-byte aligned
+    assert call([0, 1], maxlen=1000) == fa.ERR_INVALID_ARG         # 16 pages cannot hold 1000 rows
+    need = c.decode_layers_workspace_bytes([0, 1], 64, 4096)      # split units need partial rows
+    assert need > 0
+    assert call([0, 1], B=64, maxlen=4096, maxp=256, ws_bytes=need - 1) == fa.ERR_WORKSPACE   # too small
+    assert call([0, 1], B=64, maxlen=4096, maxp=256, ws_bytes=need, ws_off=16) == fa.ERR_INVALID_ARG   # unaligned
+    assert call([0, 1], B=0) == fa.OK                              # an empty batch is a no-op
