@@ -223,3 +223,25 @@ def test_multi_layer_decode_argument_checks(fa):
     assert call([0, 1], B=64, maxlen=4096, maxp=256, ws_bytes=need - 1) == fa.ERR_WORKSPACE   # too small
     assert call([0, 1], B=64, maxlen=4096, maxp=256, ws_bytes=need, ws_off=16) == fa.ERR_INVALID_ARG   # unaligned
     assert call([0, 1], B=0) == fa.OK                              # an empty batch is a no-op
+
+
+def test_extend_argument_checks(fa):
+    """fa_paged_extend_attn / fa_paged_decode_multi_attn refuse what they cannot
+    serve before touching the device: negative sizes, query heads per KV head
+    that do not divide the 128-row tile, an unbound slab; an empty call is a
+    no-op."""
+    lib = fa.lib()
+    c = fa.Cache([lay(FULL, 256, 6, 2)], 64, 16)     # 3 query heads per KV head: 3 does not divide 128
+    assert lib.fa_paged_extend_attn(c._h, 0, None, None, None, None, None, None, 4, 1, 8, 8, 16, None, None,
+                                    None) == fa.ERR_UNSUPPORTED
+    assert lib.fa_paged_decode_multi_attn(c._h, 0, None, None, None, None, 4, 1, 8, 8, 16, None, None,
+                                          None) == fa.ERR_UNSUPPORTED
+    c = fa.Cache([lay(SLIDING, 256, 8, 1, 64)], 64, 16)
+    assert lib.fa_paged_extend_attn(c._h, 0, None, None, None, None, None, None, 4, -1, 8, 8, 16, None, None,
+                                    None) == fa.ERR_INVALID_ARG                       # B < 0
+    assert lib.fa_paged_extend_attn(c._h, 0, None, None, None, None, None, None, 4, 0, 0, 0, 0, None, None,
+                                    None) == fa.OK                                    # nothing to do
+    assert lib.fa_paged_extend_attn(c._h, 0, None, None, None, None, None, None, 4, 1, 8, 8, 16, None, None,
+                                    None) == fa.ERR_NOT_BOUND
+    assert lib.fa_paged_extend_attn(c._h, 3, None, None, None, None, None, None, 4, 1, 8, 8, 16, None, None,
+                                    None) == fa.ERR_INVALID_ARG                       # no layer 3
