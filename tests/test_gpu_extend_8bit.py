@@ -183,3 +183,20 @@ def test_8bit_multi_token_decode(spec, kv_dtype):
     c = Case8([layer], prefix, new, kv_dtype, seed=33, store_chunk=True)
     _check(c.decode_multi(0), c.oracle_decode_multi(0), "8-bit multi-token decode")
     assert c.fa.device_error() == 0
+
+
+EDGE = [
+    # (layer, prefix, chunk, page size)
+    (lay(W.SLIDING, 256, 8, 1, 1), [20, 0], [45, 16], 16),          # W = 1: only the current token
+    (lay(W.FULL, 256, 2, 2), [0, 129], [257, 1], 16),               # empty prefix; a single new token
+    (lay(W.SLIDING, 512, 8, 2, 40), [95, 33, 64], [33, 96, 1], 32), # page size 32
+]
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+@pytest.mark.parametrize("spec", EDGE, ids=["W1", "empty_prefix", "page32"])
+def test_8bit_extend_edges(spec, kv_dtype):
+    layer, prefix, chunk, ps = spec
+    c = Case8([layer], prefix, chunk, kv_dtype, seed=34, page_size=ps)
+    _check(c.extend(0), c.oracle_extend(0), "8-bit extend edge")
+    assert c.fa.device_error() == 0
