@@ -235,10 +235,9 @@ def test_window_pool(kv_dtype):
     q = case.q[0]
     out = torch.empty_like(q)
     indptr = torch.arange(0, case.B + 1, dtype=torch.int32, device="cuda")
-    if kv_dtype == W.KV_BF16:
-        case.cache.decode_multi(0, q, indptr, case.lens_dev, case.bt_dev[0], 1, case.max_len, out)
-        ref, _ = case.oracle_decode(0, range(case.B))
-        assert_close(out, ref, what="multi-token decode on the window pool")
+    case.cache.decode_multi(0, q, indptr, case.lens_dev, case.bt_dev[0], 1, case.max_len, out)
+    ref, _ = case.oracle_decode(0, range(case.B))
+    assert_close(out, ref, what="multi-token decode on the window pool")
     # a page id past the window pool (not past the full pool) is refused by the sliding layer
     bt = case.bt_dev[0].clone()
     L0 = int(case.lens[0])
