@@ -637,10 +637,15 @@ class PrefillStep:
 
 
 def prefill_measure(args, dev):
-    """Chunked prefill TFLOP/s on the chunked-prefill workload (extend kernel)."""
+    """Chunked prefill TFLOP/s on the chunked-prefill workload (extend kernel),
+    its slabs in the format --prefill-kv names (bf16 by default)."""
+    import dataclasses
     import torch
     import full_attention_gb300 as fa
     w = W.chunked_prefill()
+    kv = {"bf16": W.KV_BF16, "int8": W.KV_INT8, "fp8": W.KV_FP8}[getattr(args, "prefill_kv", "bf16")]
+    if kv != w.kv_dtype:
+        w = dataclasses.replace(w, kv_dtype=kv)
     step = PrefillStep(w, dev)
     for _ in range(3):
         step.run()
@@ -699,13 +704,15 @@ def prefill_measure(args, dev):
             "tflops": round(fl / tl / 1e12, 1), "ms": round(tl * 1e3, 4),
             "executed_flop_factor": 1.5 if d["head_dim"] == 512 else 1.0}
     achieved = step.total_flops / ext_t / 1e12
-    return {"workload": w.name, "value": round(step.total_flops / t / 1e12, 1), "unit": "TFLOP/s",
+    return {"workload": w.name, "kv_format": getattr(args, "prefill_kv", "bf16"),
+            "value": round(step.total_flops / t / 1e12, 1), "unit": "TFLOP/s",
             "ms_per_prefill": round(t * 1e3, 4), "tokens_per_s": round(step.tokens / t, 1),
             "algorithmic_tflop": round(step.total_flops / 1e12, 4),
             "roofline": {"kernel": "extend_kernel (tcgen05 chunked prefill)", "bound": "tensor",
                          "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                          "frac": round(achieved / bf16, 3), "peak_source": src + " (dense bf16 burst)",
-                         "traffic": profiled_traffic("extend_chunked_prefill",
+                         "traffic": profiled_traffic("extend_chunked_prefill" + ("" if kv == W.KV_BF16 else
+                                                                                   "_" + args.prefill_kv),
                                                      source_digest("fa_extend.cu", "fa_ptx.cuh")),
                          "algorithmic_flop_per_launch": round(step.total_flops / (step.nchunks * nl)),
                          "per_layer": per_layer},
@@ -868,6 +875,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=20)
+    ap.add_argument("--prefill-kv", default="bf16", choices=["bf16", "int8", "fp8"],
+                    help="slab format of the chunked-prefill measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
