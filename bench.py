@@ -419,12 +419,96 @@ def gpu_arm(args, rank, world):
     e2["h2d_bytes_per_step"] = int(reduce_over_ranks(e2["h2d_bytes_per_step"], "sum", world, dev))
     e2["d2h_bytes_per_step"] = int(reduce_over_ranks(e2["d2h_bytes_per_step"], "sum", world, dev))
     res["e2e"] = e2
+    if args.workload == "tiny_decode":
+        res["config"]["role"] = "parity only: latency-bound (about 26 KB per step); GB/s is not a roofline figure"
+        res["roofline"]["frac"] = None
     if rank == 0:
         if args.workload == "e2b_decode" and not args.no_prefill:
             res["prefill"] = prefill_measure(args, dev)
+        if args.workload == "e2b_decode" and not args.no_subrecords:
+            # the other decode workloads, driver-observed: long context, int8,
+            # fp8 (configs 4 and 5, and 5 in the fp8 format) and the tiny one
+            del step
+            torch.cuda.empty_cache()
+            res["workloads"] = {n: decode_subrecord(n, args, dev, flush)
+                                for n in ("long_decode", "int8_decode", "fp8_decode", "tiny_decode")}
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
         print(json.dumps(res), flush=True)
+
+
+def time_graph(torch, fn, flush, n):
+    """Capture fn() in a CUDA graph (eager if capture fails) and return its
+    mean device time in seconds over n replays, L2 flushed before each."""
+    g = None
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+    except Exception as e:
+        print(f"# graph capture failed ({e}); timing eager launches", file=sys.stderr)
+        torch.cuda.synchronize()
+        g = None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    for _ in range(n):
+        flush.zero_()
+        e0.record()
+        g.replay() if g is not None else fn()
+        e1.record()
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    return tot / n / 1e3, g is not None
+
+
+def decode_subrecord(name, args, dev, flush):
+    """A compact record of another decode workload (the same 12-layer step,
+    per-layer launches in a graph, L2 flushed before every step): GB/s against
+    the measured HBM peak, and the oracle on a sample of it.  The tiny
+    workload moves 26 KB per step: it is a parity case, so it gets its
+    latency only."""
+    import torch
+    import full_attention_gb300 as fa
+    w = W.ALL[name]()
+    step = DecodeStep(w, dev)
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    n = max(5, min(args.steps, 100))
+    t, graphed = time_graph(torch, step.run, flush, n)
+    tm, _ = time_graph(torch, step.run_layers, flush, n)
+    assert fa.device_error() == 0
+    hbm = measured_peaks()[0]
+    rec = {"workload": w.name, "ms_per_step": round(t * 1e3, 4), "tokens_per_s": round(step.B / t, 1),
+           "dtype": {W.KV_BF16: "bf16", W.KV_INT8: "int8", W.KV_FP8: "fp8"}[w.kv_dtype],
+           "steps": n, "graph": graphed, "l2": "flushed before every step (256 MiB write)"}
+    if name == "tiny_decode":
+        rec.update({"role": "parity only: latency-bound (about 26 KB per step), no bandwidth figure",
+                    "unit": "ms per step", "value": rec["ms_per_step"]})
+    else:
+        gbs = step.step_bytes / t / 1e9
+        rec.update({"value": round(gbs, 1), "unit": "GB/s", "pct_of_peak": round(100 * gbs / hbm, 1),
+                    "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                                 "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 3),
+                                 "algorithmic_bytes_per_launch": round(step.step_bytes / len(step.layers)),
+                                 "traffic": profiled_traffic(f"decode_{name}", source_digest("fa_decode.cu",
+                                                                                            "fa_ptx.cuh"))},
+                    "multi_layer_step": {"ms_per_step": round(tm * 1e3, 4),
+                                         "unique_gb_per_s": round(step.unique_bytes / tm / 1e9, 1),
+                                         "frac_unique_of_peak": round(step.unique_bytes / tm / 1e9 / hbm, 3)}})
+    if not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(name, min(args.cpu_seconds, 6.0))
+    del step
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
 
 def multi_layer_measure(step, args, torch, flush, hbm):
@@ -480,13 +564,19 @@ def multi_layer_measure(step, args, torch, flush, hbm):
             "launches_per_step": 1 + len(step.groups), "graph": g is not None}
 
 
-def _arena(torch, tensors, device, pinned):
-    """One byte buffer holding `tensors` end to end (256-byte aligned pieces);
-    returns (buffer, views with the tensors' shapes and dtypes)."""
+def _arena_offsets(tensors):
+    """Byte offsets of `tensors` laid end to end in 256-byte aligned pieces, and the total."""
     offs, n = [], 0
     for t in tensors:
         offs.append(n)
         n += (t.numel() * t.element_size() + 255) // 256 * 256
+    return offs, n
+
+
+def _arena(torch, tensors, device, pinned):
+    """One byte buffer holding `tensors` end to end (256-byte aligned pieces);
+    returns (buffer, views with the tensors' shapes and dtypes)."""
+    offs, n = _arena_offsets(tensors)
     buf = torch.empty(max(n, 1), dtype=torch.uint8, device=device)
     if pinned:
         buf = buf.pin_memory()
@@ -496,10 +586,13 @@ def _arena(torch, tensors, device, pinned):
 
 def e2e_decode(step, args, torch):
     """Same metric through the public API with host buffers: every step copies
-    all of its inputs (queries, new k/v rows, slots, lengths, tables) from one
-    pinned host buffer into the device buffer the calls read, runs the step,
-    and reads every layer's output back into one pinned host buffer (one copy
-    each way; the library calls read and write views of those buffers)."""
+    all of its inputs (queries, new k/v rows, slots, lengths, tables) from a
+    pinned host buffer into a device buffer the calls read (one copy), runs
+    the step, and reads every layer's output back into a pinned host buffer
+    (one copy).  Two device buffers alternate between steps, and the copies
+    run on two copy streams ordered by events, so a step's copies overlap the
+    neighbouring steps' compute; every step's copies lie inside the timed
+    region, which spans all steps."""
     dev = step.device
     keys = [("q", i) for i in sorted(step.q)] + [("new", i, j) for i in sorted(step.new) for j in range(3)] + \
         [("bt", i) for i in sorted(step.bt)] + [("lens",)]
@@ -515,47 +608,75 @@ def e2e_decode(step, args, torch):
 
     saved = (dict(step.q), dict(step.new), dict(step.bt), step.lens_dev, dict(step.out))
     srcs = [get(k) for k in keys]
-    d_in, d_views = _arena(torch, srcs, dev, False)
+    outs = [step.out[i] for i in sorted(step.out)]
     h_in, h_views = _arena(torch, [t.cpu() for t in srcs], "cpu", True)
     for hv, t in zip(h_views, srcs):
         hv.copy_(t.cpu())
-    outs = [step.out[i] for i in sorted(step.out)]
-    d_out, d_oviews = _arena(torch, outs, dev, False)
-    h_out, _ = _arena(torch, [t.cpu() for t in outs], "cpu", True)
-    new = {}
-    for k, v in zip(keys, d_views):
-        if k[0] == "q":
-            step.q[k[1]] = v
-        elif k[0] == "new":
-            new.setdefault(k[1], [None] * 3)[k[2]] = v
-        elif k[0] == "bt":
-            step.bt[k[1]] = v
-        else:
-            step.lens_dev = v
-    step.new = {i: tuple(v) for i, v in new.items()}
-    step.out = {i: v for i, v in zip(sorted(saved[4]), d_oviews)}
+    bufs = []
+    for _ in range(2):
+        d_in, d_views = _arena(torch, srcs, dev, False)
+        d_out, d_oviews = _arena(torch, outs, dev, False)
+        h_out, _ = _arena(torch, [t.cpu() for t in outs], "cpu", True)
+        views = {"q": {}, "new": {}, "bt": {}, "lens": None}
+        for k, v in zip(keys, d_views):
+            if k[0] == "q":
+                views["q"][k[1]] = v
+            elif k[0] == "new":
+                views["new"].setdefault(k[1], [None] * 3)[k[2]] = v
+            elif k[0] == "bt":
+                views["bt"][k[1]] = v
+            else:
+                views["lens"] = v
+        views["new"] = {i: tuple(v) for i, v in views["new"].items()}
+        views["out"] = {i: v for i, v in zip(sorted(saved[4]), d_oviews)}
+        bufs.append((d_in, d_out, h_out, views, d_oviews))
     bi = int(h_in.numel())
-    bo = int(h_out.numel())
+    bo = int(bufs[0][2].numel())
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cs = torch.cuda.current_stream()
+    xs_in, xs_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(3, min(args.steps, 200))
-    tot = 0.0
-    try:
-        for it in range(n + 2):
-            flush.zero_()
-            e0.record()
+
+    def one_step(i):
+        b = i % 2
+        d_in, d_out, h_out, views, _ = bufs[b]
+        with torch.cuda.stream(xs_in):   # this step's inputs, once buffer b's last user is done
+            xs_in.wait_event(ev["done"][b])
             d_in.copy_(h_in, non_blocking=True)
-            step.run()
+            ev["in"][b].record(xs_in)
+        cs.wait_event(ev["in"][b])
+        cs.wait_event(ev["out"][b])      # buffer b's previous outputs have been read back
+        step.q, step.new, step.bt, step.lens_dev, step.out = (views["q"], views["new"], views["bt"], views["lens"],
+                                                              views["out"])
+        step.run()
+        ev["done"][b].record(cs)
+        with torch.cuda.stream(xs_out):
+            xs_out.wait_event(ev["done"][b])
             h_out.copy_(d_out, non_blocking=True)
-            e1.record()
-            e1.synchronize()
-            if it >= 2:
-                tot += e0.elapsed_time(e1)
-        # the outputs read back are the step's: compare with the device-resident path
-        got = [h_out[o.data_ptr() - d_out.data_ptr():][: t.numel() * t.element_size()].clone()
-               for o, t in zip(d_oviews, outs)]
+            ev["out"][b].record(xs_out)
+
+    try:
+        for i in range(4):               # warm-up of the pipeline
+            one_step(i)
+        torch.cuda.synchronize()
+        flush.zero_()
+        e0.record(cs)
+        xs_in.wait_stream(cs)
+        xs_out.wait_stream(cs)
+        for i in range(n):
+            one_step(i)
+        cs.wait_stream(xs_out)
+        e1.record(cs)
+        e1.synchronize()
+        tot = e0.elapsed_time(e1)
+        last = bufs[(n - 1) % 2]
+        got = [last[2][o.data_ptr() - last[1].data_ptr():][: t.numel() * t.element_size()].clone()
+               for o, t in zip(last[4], outs)]
     finally:
         step.q, step.new, step.bt, step.lens_dev, step.out = saved
+    # the outputs read back are the step's: compare with the device-resident path
     step.run()
     torch.cuda.synchronize()
     for g, t in zip(got, outs):
@@ -563,7 +684,8 @@ def e2e_decode(step, args, torch):
     t = tot / n / 1e3
     return {"value": round(step.step_bytes / t / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": t * 1e3,
-            "path": "C-ABI calls; one host-to-device and one device-to-host copy per step (pinned buffers)"}
+            "path": "C-ABI calls; per step one host-to-device and one device-to-host copy (pinned buffers), "
+                    "double-buffered on two copy streams so copies overlap the neighbouring steps"}
 
 
 def visible_pairs(kind, window, P, n):
@@ -609,7 +731,7 @@ class PrefillStep:
                 q = W.randn_bf16((B * C, d["num_q_heads"], d["head_dim"]), s0, device)
                 k = W.randn_bf16((B * C, d["num_kv_heads"], d["head_dim"]), s0 + 1, device)
                 v = W.randn_bf16((B * C, d["num_kv_heads"], d["head_dim"]), s0 + 2, device)
-                row.append((q, k, v, torch.from_numpy(slots).to(device)))
+                row.append((q, k, v, torch.from_numpy(slots).to(device), self.prefix[c], self.indptr))
                 fl.append(4.0 * d["head_dim"] * d["num_q_heads"] * B *
                           visible_pairs(d["kind"], d["window"], P, C))
             self.inputs.append(row)
@@ -623,22 +745,47 @@ class PrefillStep:
     def launches(self):
         return self.nchunks * len(self.w.layers) * 2
 
-    def run(self, events=None):
+    def store_bytes(self, li):
+        """Bytes one chunk store of layer li must move: the chunk's bf16 k, v
+        rows read, their slab rows (and 8-bit scales) written."""
+        d = self.w.layers[li]
+        q8 = self.w.kv_dtype != W.KV_BF16
+        rows = self.w.batch * self.w.chunk * d["num_kv_heads"] * 2
+        return rows * (d["head_dim"] * 2 + d["head_dim"] * (1 if q8 else 2) + (4 if q8 else 0)) + \
+            self.w.batch * self.w.chunk * 4
+
+    def run(self, events=None, store_events=None, inputs=None, outs=None, per_chunk=None):
+        """One prefill: per chunk and layer the store of the chunk rows, then
+        extend.  `inputs`/`outs` replace the device-resident tensors (the
+        end-to-end path); per_chunk(c, phase) runs before ("in") and after
+        ("out") each chunk's calls."""
         C = self.w.chunk
+        inputs = self.inputs if inputs is None else inputs
         for c in range(self.nchunks):
+            if per_chunk is not None:
+                per_chunk(c, "in")
             for li in range(len(self.w.layers)):
-                q, k, v, slots = self.inputs[c][li]
+                q, k, v, slots, prefix, indptr = inputs[c][li]
+                if store_events is not None:
+                    store_events[c][li][0].record()
                 self.cache.store(li, k, v, slots)
+                if store_events is not None:
+                    store_events[c][li][1].record()
                 if events is not None:
                     events[c][li][0].record()
-                self.cache.extend(li, q, k, v, self.indptr, self.prefix[c], self.bt, C, self.nchunks * C, self.out[li])
+                out = self.out[li] if outs is None else outs[c][li]
+                self.cache.extend(li, q, k, v, indptr, prefix, self.bt, C, self.nchunks * C, out)
                 if events is not None:
                     events[c][li][1].record()
+            if per_chunk is not None:
+                per_chunk(c, "out")
 
 
 def prefill_measure(args, dev):
     """Chunked prefill TFLOP/s on the chunked-prefill workload (extend kernel),
-    its slabs in the format --prefill-kv names (bf16 by default)."""
+    its slabs in the format --prefill-kv names (bf16 by default); the chunk
+    stores' GB/s; the same prefill end to end from host buffers; the oracle's
+    rate on a sample of the same workload."""
     import dataclasses
     import torch
     import full_attention_gb300 as fa
@@ -652,19 +799,22 @@ def prefill_measure(args, dev):
     torch.cuda.synchronize()
     assert fa.device_error() == 0
     nl = len(w.layers)
-    events = [[(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nl)] for _ in range(step.nchunks)]
 
-    def capture(ev):
+    def ev_grid():
+        return [[(torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True)) for _ in range(nl)] for _ in range(step.nchunks)]
+    events, store_events = ev_grid(), ev_grid()
+
+    def capture(ev, sev):
         try:
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(s):
-                step.run(ev)
+                step.run(ev, sev)
             torch.cuda.current_stream().wait_stream(s)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                step.run(ev)
+                step.run(ev, sev)
             torch.cuda.synchronize()
             return g
         except Exception as e:
@@ -672,7 +822,7 @@ def prefill_measure(args, dev):
             torch.cuda.synchronize()
             return None
 
-    g_plain, g_ev = capture(None), capture(events)
+    g_plain, g_ev = capture(None, None), capture(events, store_events)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(3, min(args.prefill_steps, 50))
@@ -686,15 +836,17 @@ def prefill_measure(args, dev):
         tot += e0.elapsed_time(e1)
     t = tot / reps / 1e3
     ext_ms = [[0.0] * nl for _ in range(step.nchunks)]
+    st_ms = [[0.0] * nl for _ in range(step.nchunks)]
     for _ in range(reps):
         flush.zero_()
-        g_ev.replay() if g_ev is not None else step.run(events)
+        g_ev.replay() if g_ev is not None else step.run(events, store_events)
         torch.cuda.synchronize()
         for c in range(step.nchunks):
             for li in range(nl):
                 ext_ms[c][li] += events[c][li][0].elapsed_time(events[c][li][1]) / reps
+                st_ms[c][li] += store_events[c][li][0].elapsed_time(store_events[c][li][1]) / reps
     assert fa.device_error() == 0
-    _, bf16, bf16s, src = measured_peaks()
+    hbm, bf16, bf16s, src = measured_peaks()
     ext_t = sum(sum(r) for r in ext_ms) / 1e3
     per_layer = {}
     for li, d in enumerate(w.layers):
@@ -704,19 +856,120 @@ def prefill_measure(args, dev):
             "tflops": round(fl / tl / 1e12, 1), "ms": round(tl * 1e3, 4),
             "executed_flop_factor": 1.5 if d["head_dim"] == 512 else 1.0}
     achieved = step.total_flops / ext_t / 1e12
-    return {"workload": w.name, "kv_format": getattr(args, "prefill_kv", "bf16"),
-            "value": round(step.total_flops / t / 1e12, 1), "unit": "TFLOP/s",
-            "ms_per_prefill": round(t * 1e3, 4), "tokens_per_s": round(step.tokens / t, 1),
-            "algorithmic_tflop": round(step.total_flops / 1e12, 4),
-            "roofline": {"kernel": "extend_kernel (tcgen05 chunked prefill)", "bound": "tensor",
-                         "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
-                         "frac": round(achieved / bf16, 3), "peak_source": src + " (dense bf16 burst)",
-                         "traffic": profiled_traffic("extend_chunked_prefill" + ("" if kv == W.KV_BF16 else
-                                                                                   "_" + args.prefill_kv),
-                                                     source_digest("fa_extend.cu", "fa_ptx.cuh")),
-                         "algorithmic_flop_per_launch": round(step.total_flops / (step.nchunks * nl)),
-                         "per_layer": per_layer},
-            "gpu_launches_per_prefill": step.launches(), "graph": g_plain is not None}
+    # the chunk stores (store_kernel), each event-bracketed: algorithmic bytes / time
+    st_bytes = sum(step.store_bytes(li) for li in range(nl)) * step.nchunks
+    st_t = sum(sum(r) for r in st_ms) / 1e3
+    store = {"kernel": "store_kernel (chunk rows into the paged slab)", "bound": "hbm",
+             "achieved": round(st_bytes / st_t / 1e9, 1), "peak": hbm, "unit": "GB/s",
+             "frac": round(st_bytes / st_t / 1e9 / hbm, 3), "peak_source": src,
+             "bytes_per_call": {("sliding D256" if d["kind"] == W.SLIDING else "full D512"): step.store_bytes(li)
+                                for li, d in enumerate(w.layers)},
+             "us_per_call": round(st_t / (step.nchunks * nl) * 1e6, 2),
+             "traffic": profiled_traffic("store_chunked_prefill", source_digest("fa_store.cu", "fa_row.cuh"))}
+    res = {"workload": w.name, "kv_format": getattr(args, "prefill_kv", "bf16"),
+           "value": round(step.total_flops / t / 1e12, 1), "unit": "TFLOP/s",
+           "ms_per_prefill": round(t * 1e3, 4), "tokens_per_s": round(step.tokens / t, 1),
+           "algorithmic_tflop": round(step.total_flops / 1e12, 4),
+           "roofline": {"kernel": "extend_kernel (tcgen05 chunked prefill)", "bound": "tensor",
+                        "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
+                        "frac": round(achieved / bf16, 3), "peak_source": src + " (dense bf16 burst)",
+                        "traffic": profiled_traffic("extend_chunked_prefill" + ("" if kv == W.KV_BF16 else
+                                                                                  "_" + args.prefill_kv),
+                                                    source_digest("fa_extend.cu", "fa_ptx.cuh")),
+                        "algorithmic_flop_per_launch": round(step.total_flops / (step.nchunks * nl)),
+                        "per_layer": per_layer},
+           "store": store,
+           "gpu_launches_per_prefill": step.launches(), "graph": g_plain is not None}
+    res["e2e"] = e2e_prefill(step, args, torch, flush)
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = prefill_cpu_baseline(w, args.cpu_seconds)
+    return res
+
+
+def e2e_prefill(step, args, torch, flush):
+    """The prefill through the public API from host buffers: per chunk one
+    host-to-device copy of that chunk's inputs (q, k, v and slots of both
+    layers, the prefix lengths, the chunk offsets) from one pinned host
+    buffer, the stores and extends reading the copied views, and one
+    device-to-host copy of the chunk's outputs into one pinned host buffer.
+    The copies run on two copy streams, ordered by events, so chunk c + 1's
+    inputs and chunk c - 1's outputs move while chunk c computes; all of a
+    prefill's copies lie inside the timed region."""
+    import full_attention_gb300 as fa
+    nl = len(step.w.layers)
+    nc = step.nchunks
+    order = [(c, li, j) for c in range(nc) for li in range(nl) for j in range(6)]
+    srcs = [step.inputs[c][li][j] for c, li, j in order]
+    offs, n_in = _arena_offsets(srcs)
+    d_in, d_views = _arena(torch, srcs, step.device, False)
+    h_in, h_views = _arena(torch, [x.cpu() for x in srcs], "cpu", True)
+    for hv, x in zip(h_views, srcs):
+        hv.copy_(x.cpu())
+    views = {k: v for k, v in zip(order, d_views)}
+    inputs = [[tuple(views[(c, li, j)] for j in range(6)) for li in range(nl)] for c in range(nc)]
+    outs_t = [step.out[li] for c in range(nc) for li in range(nl)]
+    ooffs, n_out = _arena_offsets(outs_t)
+    d_out, d_oviews = _arena(torch, outs_t, step.device, False)
+    h_out, _ = _arena(torch, [x.cpu() for x in outs_t], "cpu", True)
+    outs = [[d_oviews[c * nl + li] for li in range(nl)] for c in range(nc)]
+    # byte range of each chunk in the two arenas
+    in_rng = [(offs[c * nl * 6], offs[(c + 1) * nl * 6] if c + 1 < nc else n_in) for c in range(nc)]
+    out_rng = [(ooffs[c * nl], ooffs[(c + 1) * nl] if c + 1 < nc else n_out) for c in range(nc)]
+    cs = torch.cuda.current_stream()
+    xs_in, xs_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(nc)] for k in ("in", "done", "out")}
+
+    def one_prefill():
+        with torch.cuda.stream(xs_in):   # every chunk's inputs, each once its last reader is done
+            for c in range(nc):
+                a, b = in_rng[c]
+                xs_in.wait_event(ev["done"][c])
+                d_in[a:b].copy_(h_in[a:b], non_blocking=True)
+                ev["in"][c].record(xs_in)
+
+        def per_chunk(c, phase):
+            if phase == "in":
+                cs.wait_event(ev["in"][c])
+                cs.wait_event(ev["out"][c])   # the previous prefill's chunk-c outputs were read back
+            else:
+                ev["done"][c].record(cs)
+                with torch.cuda.stream(xs_out):
+                    xs_out.wait_event(ev["done"][c])
+                    a, b = out_rng[c]
+                    h_out[a:b].copy_(d_out[a:b], non_blocking=True)
+                    ev["out"][c].record(xs_out)
+
+        step.run(inputs=inputs, outs=outs, per_chunk=per_chunk)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(args.prefill_steps, 20))
+    for _ in range(2):
+        one_prefill()
+    torch.cuda.synchronize()
+    flush.zero_()
+    e0.record(cs)
+    xs_in.wait_stream(cs)
+    xs_out.wait_stream(cs)
+    for _ in range(n):
+        one_prefill()
+    cs.wait_stream(xs_out)
+    e1.record(cs)
+    e1.synchronize()
+    tot = e0.elapsed_time(e1)
+    # the last chunk's outputs read back equal the device-resident prefill's
+    step.run()
+    torch.cuda.synchronize()
+    assert fa.device_error() == 0
+    for li in range(nl):
+        o = step.out[li]
+        nb = o.numel() * o.element_size()
+        got = h_out[ooffs[(nc - 1) * nl + li]:][:nb]
+        assert torch.equal(got, o.contiguous().view(torch.uint8).view(-1).cpu()), "end-to-end prefill output differs"
+    t = tot / n / 1e3
+    return {"value": round(step.total_flops / t / 1e12, 1), "unit": "TFLOP/s", "h2d_bytes_per_step": int(n_in),
+            "d2h_bytes_per_step": int(n_out), "ms_per_step": round(t * 1e3, 4),
+            "path": "C-ABI store + extend calls; per chunk one host-to-device and one device-to-host copy "
+                    "(pinned buffers) on two copy streams overlapping the compute; a step is one whole prefill"}
 
 
 # ----------------------------------------------------------------------------
@@ -776,24 +1029,87 @@ def _oracle_worker(conn, name, units, seed):
         conn.send((t, nb))
 
 
+def _extend_oracle_worker(conn, kv_dtype, units, seed):
+    """A spawned process for the chunked-prefill workload: it holds seeded
+    inputs for its (chunk, layer) units (one sequence each, prefix c * chunk,
+    a whole chunk of new tokens) and on each request runs the extend oracle on
+    the next n of them, for 4 random tokens of the chunk and every query head;
+    only the oracle calls are timed.  Replies (seconds, flops)."""
+    import oracle
+    w = W.chunked_prefill()
+    C, ps = w.chunk, w.page_size
+    r = W.rng(seed)
+    data = []
+    for c, li in units:
+        d = dict(w.layers[li], kv_source=W.KV_OWN)
+        P = c * C
+        npg = max(1, (P + ps - 1) // ps)
+        shape = (npg, d["num_kv_heads"], ps, d["head_dim"])
+        if kv_dtype == W.KV_BF16:
+            slab = (_bf16_normal(r, shape), _bf16_normal(r, shape))
+        elif kv_dtype == W.KV_INT8:
+            sc = (r.random(shape[:3], dtype=np.float32) * 0.03).astype(np.float32)
+            slab = (r.integers(-127, 128, size=shape, dtype=np.int8), r.integers(-127, 128, size=shape, dtype=np.int8),
+                    sc, sc.copy())
+        else:
+            sc = (r.random(shape[:3], dtype=np.float32) * 0.01).astype(np.float32)
+            codes = [r.integers(0, 254, size=shape, dtype=np.uint8) for _ in range(2)]
+            slab = tuple(np.where(x >= 0x7F, x + 1, x).astype(np.uint8) for x in codes) + (sc, sc.copy())
+        q = _bf16_normal(r, (C, d["num_q_heads"], d["head_dim"]))
+        kx = _bf16_normal(r, (C, d["num_kv_heads"], d["head_dim"]))
+        vx = _bf16_normal(r, (C, d["num_kv_heads"], d["head_dim"]))
+        data.append((d, slab, q, kx, vx, P, np.arange(npg, dtype=np.int32)[None]))
+    conn.send("ready")
+    k = 0
+    while True:
+        n = conn.recv()
+        if n is None:
+            break
+        t = fl = 0.0
+        for _ in range(n):
+            d, slab, q, kx, vx, P, bt = data[k % len(data)]
+            k += 1
+            toks = sorted(r.choice(C, size=4, replace=False).tolist())
+            rows = [(tt, j) for tt in toks for j in range(d["num_q_heads"])]
+            t0 = time.perf_counter()
+            oracle.paged_extend([d], 0, {0: slab}, q, kx, vx, np.array([0, C], np.int32), np.array([P], np.int32),
+                                bt, ps, rows=rows)
+            t += time.perf_counter() - t0
+            for tt in toks:
+                vis = min(d["window"], P + tt + 1) if d["kind"] == W.SLIDING else P + tt + 1
+                fl += 4.0 * d["head_dim"] * d["num_q_heads"] * vis
+        conn.send((t, fl))
+
+
 class OraclePool:
     """One spawned oracle process per host core, each owning a share of the
-    workload's (sequence, layer) units.  Spawned, never forked, so it is safe
-    after CUDA is initialised."""
+    workload's units: (sequence, layer) pairs of a decode workload, or
+    (chunk, layer) pairs of the chunked-prefill workload.  Spawned, never
+    forked, so it is safe after CUDA is initialised."""
 
-    def __init__(self, name, procs=None, seed=0):
+    def __init__(self, name, procs=None, seed=0, prefill_kv=None):
         for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[var] = "1"   # one thread per process: `cores` counts processes
-        w = W.ALL[name]()
-        B = len(W.seq_lens(w))
-        units = [(b, li) for b in range(B) for li in range(len(w.layers))]
-        self.procs = max(1, min(procs or os.cpu_count() or 1, len(units)))
+        if prefill_kv is None:
+            w = W.ALL[name]()
+            B = len(W.seq_lens(w))
+            units = [(b, li) for b in range(B) for li in range(len(w.layers))]
+        else:
+            w = W.chunked_prefill()
+            units = [(c, li) for c in range(w.prompt_len // w.chunk) for li in range(len(w.layers))]
+        self.procs = max(1, min(procs or os.cpu_count() or 1, len(units) if prefill_kv is None else 10 ** 6))
         self.units = len(units)
         ctx = mp.get_context("spawn")
         self.conns, self.ps = [], []
         for i in range(self.procs):
             a, b = ctx.Pipe()
-            p = ctx.Process(target=_oracle_worker, args=(b, name, units[i::self.procs], seed + i), daemon=True)
+            if prefill_kv is None:
+                target, pargs = _oracle_worker, (b, name, units[i::self.procs], seed + i)
+            else:
+                # every process holds two of the (chunk, layer) units, spread over all chunks
+                mine = [units[(2 * i + j) % len(units)] for j in range(2)]
+                target, pargs = _extend_oracle_worker, (b, prefill_kv, mine, seed + i)
+            p = ctx.Process(target=target, args=pargs, daemon=True)
             p.start()
             self.conns.append(a)
             self.ps.append(p)
@@ -831,6 +1147,35 @@ def cpu_baseline(name, seconds):
     return {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": pool.procs, "kind": "oracle",
             "sample": f"the whole step ({len(W.seq_lens(w))} sequences x {len(w.layers)} layers) x {reps}, "
                       f"fp64 numpy oracle, {pool.procs} processes, {t:.2f} s of oracle wall time"}
+
+
+def prefill_cpu_baseline(w, seconds):
+    """The extend oracle on a seeded sample of the chunked-prefill workload:
+    every process takes (chunk, layer) units spread over all chunks and both
+    layers and computes 4 random tokens x every query head per unit, until
+    about `seconds` of oracle time; the rate (algorithmic flops of the rows
+    computed / the busiest process's time) extrapolates linearly to the whole
+    prefill."""
+    pool = OraclePool(w.name, prefill_kv=w.kv_dtype)
+    try:
+        fl, t = pool.run(2)
+        reps = 1
+        while t < seconds * 2 / 3 and reps < 64:
+            f2, t2 = pool.run(2)
+            fl, t, reps = fl + f2, t + t2, reps + 1
+    finally:
+        pool.close()
+    step_flops = 0.0
+    for d in w.layers:
+        for c in range(w.prompt_len // w.chunk):
+            step_flops += 4.0 * d["head_dim"] * d["num_q_heads"] * w.batch * visible_pairs(d["kind"], d["window"],
+                                                                                          c * w.chunk, w.chunk)
+    rate = fl / t
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": pool.procs, "kind": "oracle",
+            "sample": f"{2 * reps} (chunk, layer) units per process x 4 random tokens x every query head, spread "
+                      f"over all 8 chunks and both layers, fp64 numpy oracle, {pool.procs} processes, "
+                      f"{t:.2f} s of oracle wall time; the whole prefill ({step_flops / 1e12:.3f} TFLOP) would "
+                      f"take about {step_flops / rate:.0f} s at this rate (linear extrapolation by flops)"}
 
 
 def reference_arm(args, rank, world):
@@ -873,6 +1218,8 @@ def main():
                                                                   "fp8_decode", "tiny_decode"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="skip the long-context, int8, fp8 and tiny decode records of the default run")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--prefill-kv", default="bf16", choices=["bf16", "int8", "fp8"],

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import weakref
 
 import torch
 
@@ -18,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
 FULL, SLIDING = 0, 1
 KV_BF16, KV_INT8, KV_FP8 = 0, 1, 2
 KV_OWN, KV_AUTO = -1, -2
-DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE = 1, 2, 4, 8, 16
+DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE, DEV_ERR_RANGE = 1, 2, 4, 8, 16, 32
+MAX_CACHES = 4096
 
 FLAG_EARLY_METADATA = 1
 
@@ -64,7 +66,7 @@ def _load() -> ctypes.CDLL:
         "fa_decode_layers_workspace_bytes": (sz, [vp, i32, vp, i32, i32]),
         "fa_paged_decode_attn_layers": (i32, [vp, i32, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_extend_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
-        "fa_get_device_error": (i32, [ctypes.POINTER(i32), vp]),
+        "fa_get_device_error": (i32, [vp, ctypes.POINTER(i32), vp]),
         "fa_last_error": (ctypes.c_char_p, []),
         "fa_status_string": (ctypes.c_char_p, [i32]),
         "fa_version": (i32, []),
@@ -77,6 +79,7 @@ def _load() -> ctypes.CDLL:
 
 
 _lib = _load()
+_live = weakref.WeakSet()   # every Cache not yet destroyed (for device_error())
 
 
 def lib() -> ctypes.CDLL:
@@ -129,12 +132,20 @@ class Cache:
                                     ctypes.byref(h)))
         self._h = h
         self._slabs = {}
+        _live.add(self)
 
     def __del__(self):
         h = getattr(self, "_h", None)
         if h is not None and _lib is not None:
             _lib.fa_cache_destroy(h)
             self._h = None
+
+    def device_error(self, stream=None) -> int:
+        """fa_get_device_error: synchronise the stream, then read and clear this
+        cache's device error word (FA_DEV_ERR_* bits of its calls' kernels)."""
+        code = ctypes.c_int32()
+        _check(_lib.fa_get_device_error(self._h, ctypes.byref(code), _s(stream)))
+        return code.value
 
     def set_flags(self, flags: int) -> None:
         """FA_FLAG_* options; FLAG_EARLY_METADATA lets kernels read index
@@ -264,10 +275,13 @@ class Cache:
 
 
 def device_error(stream=None) -> int:
-    """Synchronise the stream, then read and clear the device error word (FA_DEV_ERR_* bits)."""
-    code = ctypes.c_int32()
-    _check(_lib.fa_get_device_error(ctypes.byref(code), _s(stream)))
-    return code.value
+    """The OR of every live cache's device error word, each read and cleared
+    (Cache.device_error) after synchronising the stream."""
+    code = 0
+    for c in list(_live):
+        if getattr(c, "_h", None) is not None:
+            code |= c.device_error(stream)
+    return code
 
 
 def workspace(nbytes: int, device="cuda"):

@@ -44,6 +44,26 @@ int sm_count() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Slots of the per-device error-word array: each live cache holds one.
+static std::mutex g_slot_mu;
+static bool g_slot_used[FA_MAX_CACHES];
+
+static int take_err_slot() {
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  for (int i = 0; i < FA_MAX_CACHES; ++i)
+    if (!g_slot_used[i]) {
+      g_slot_used[i] = true;
+      return i;
+    }
+  return -1;
+}
+
+static void give_err_slot(int i) {
+  if (i < 0 || i >= FA_MAX_CACHES) return;
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  g_slot_used[i] = false;
+}
+
 // int8 and fp8 slabs: one code byte per element plus an fp32 scale per row
 static bool quantised(int kv_dtype) { return kv_dtype != FA_KV_BF16; }
 static size_t elem_bytes(int kv_dtype) { return quantised(kv_dtype) ? 1 : 2; }
@@ -256,6 +276,11 @@ fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t
     return fail(FA_ERR_UNSUPPORTED, "kv_dtype %d unsupported", kv_dtype);
   fa_cache* c = new (std::nothrow) fa_cache();
   if (!c) return fail(FA_ERR_INVALID_ARG, "out of host memory");
+  c->err_slot = take_err_slot();
+  if (c->err_slot < 0) {
+    delete c;
+    return fail(FA_ERR_UNSUPPORTED, "at most %d caches may be live at once", FA_MAX_CACHES);
+  }
   c->num_pages = num_pages;
   c->page_size = page_size;
   c->kv_dtype = kv_dtype;
@@ -280,7 +305,7 @@ fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t
     else if (static_cast<int64_t>(num_pages) * d.num_kv_heads * page_size >= (1LL << 31))
       st = fail(FA_ERR_UNSUPPORTED, "layer %d: num_pages * Hkv * page_size must stay below 2^31", i);
     if (st != FA_OK) {
-      delete c;
+      fa_cache_destroy(c);
       return st;
     }
     if (d.kv_source == FA_KV_OWN) {
@@ -299,7 +324,7 @@ fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t
     else if (c->layers[src].d.head_dim != d.head_dim || c->layers[src].d.num_kv_heads != d.num_kv_heads)
       st = fail(FA_ERR_UNSUPPORTED, "layer %d: KV geometry differs from its source %d", i, src);
     if (st != FA_OK) {
-      delete c;
+      fa_cache_destroy(c);
       return st;
     }
     L.owner = src;
@@ -308,7 +333,11 @@ fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t
   return ok();
 }
 
-void fa_cache_destroy(fa_cache* c) { delete c; }
+void fa_cache_destroy(fa_cache* c) {
+  if (!c) return;
+  give_err_slot(c->err_slot);
+  delete c;
+}
 
 fa_status fa_cache_set_flags(fa_cache* c, uint32_t flags) {
   if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
@@ -384,6 +413,10 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
     s.tm_ks = s.tm_k;   // unused in bf16; keeps the kernel parameters defined
     s.tm_vs = s.tm_v;
   }
+  // the error word this cache's kernels report into starts clean on this
+  // device (its slot may have served a cache destroyed earlier)
+  cudaError_t ce = clear_device_error_word(c);
+  if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "clearing the device error word: %s", cudaGetErrorString(ce));
   s.k = k;
   s.v = v;
   s.k_scale = quantised(c->kv_dtype) ? k_scale : nullptr;
@@ -417,7 +450,7 @@ fa_status fa_kv_store(fa_cache* c, int32_t layer, const void* k, const void* v, 
   if (!k || !v || !slot_mapping) return fail(FA_ERR_INVALID_ARG, "k, v, slot_mapping must be non-NULL");
   if (!aligned16(k) || !aligned16(v)) return fail(FA_ERR_INVALID_ARG, "k, v must be 16-byte aligned");
   cudaError_t ce;
-  unsigned int* err = device_error_word(&ce);
+  unsigned int* err = device_error_word(c, &ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   StoreArgs a{k, v, slot_mapping, s->k, s->v, s->k_scale, s->v_scale, T, L.d.num_kv_heads, L.d.head_dim,
               c->page_size, layer_pages(c, layer), c->kv_dtype, (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0, err};
@@ -441,7 +474,7 @@ fa_status fa_kv_store_layers(fa_cache* c, int32_t n, const int32_t* layers, cons
   StoreArgs a[FA_MAX_LAYERS_PER_LAUNCH];
   int m = 0;
   cudaError_t ce;
-  unsigned int* err = device_error_word(&ce);
+  unsigned int* err = device_error_word(c, &ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   for (int i = 0; i < n; ++i) {
     if ((st = check_layer(c, layers[i]))) return st;
@@ -565,7 +598,7 @@ static fa_status decode_call(fa_cache* c, int32_t layer, const void* q, const vo
   if (p.ws_bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   cudaError_t ce;
-  unsigned int* err = device_error_word(&ce);
+  unsigned int* err = device_error_word(c, &ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   (void)L;
   DecodeArgs a{};
@@ -636,7 +669,7 @@ fa_status fa_paged_decode_attn_layers(fa_cache* c, int32_t n, const int32_t* lay
   if (need && (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   cudaError_t ce;
-  unsigned int* err = device_error_word(&ce);
+  unsigned int* err = device_error_word(c, &ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   DecodeArgs a[FA_MAX_LAYERS_PER_LAUNCH];
   DecodePlan plans[FA_MAX_LAYERS_PER_LAUNCH];
@@ -679,7 +712,7 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
     return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_prefix_len %d", max_pages_per_seq,
                 max_prefix_len);
   cudaError_t ce;
-  unsigned int* err = device_error_word(&ce);
+  unsigned int* err = device_error_word(c, &ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   ExtendArgs a{};
   a.q = q;
@@ -742,7 +775,7 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   if (max_pages_per_seq < (max_seq_len + c->page_size - 1) / c->page_size)
     return fail(FA_ERR_INVALID_ARG, "max_pages_per_seq %d cannot hold max_seq_len %d", max_pages_per_seq, max_seq_len);
   cudaError_t ce;
-  unsigned int* err = device_error_word(&ce);
+  unsigned int* err = device_error_word(c, &ce);
   if (!err) return fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   ExtendArgs a{};
   a.q = q;

@@ -32,7 +32,8 @@
 // values (int8: byte permute + one subtraction; e4m3: the hardware pair
 // conversion), the K scale multiplies the fp32 scores, the V scale is folded
 // into P (normalised by the step's largest scale, which joins the running
-// rescale), and the MMAs run in fp16.
+// rescale), and the MMAs run in fp16; a query element f16 cannot hold
+// (magnitude 65536 or more) saturates to +-65504 and sets FA_DEV_ERR_RANGE.
 #include <cfloat>
 #include <climits>
 #include <mutex>
@@ -651,6 +652,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
     }
     uint32_t qf[QF][KV ? 4 : 2];
     {
+      uint32_t qbig = 0;   // 8-bit formats: a query element f16 cannot hold
       const __nv_bfloat16* qrow = qbuf + (hv ? gid : 0) * D;
 #pragma unroll
       for (int kk = 0; kk < QF; ++kk) {
@@ -663,10 +665,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
           for (int half = 0; half < 2; ++half) {
             const int d = qk_d0 + kk * 32 + half * 16 + 4 * tig;
             const uint2 w = hv ? *reinterpret_cast<const uint2*>(qrow + d) : make_uint2(0u, 0u);
-            qf[kk][2 * half + 0] = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-            qf[kk][2 * half + 1] = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+            qbig |= bf16x2_past_f16(w.x) | bf16x2_past_f16(w.y);
+            qf[kk][2 * half + 0] = pack_f16x2_sat(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+            qf[kk][2 * half + 1] = pack_f16x2_sat(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
           }
         }
+      }
+      if constexpr (KV != 0) {
+        if (__any_sync(0xffffffffu, qbig != 0) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
       }
     }
     // qbuf is refilled by a bulk copy (async proxy) once every warp has

@@ -32,11 +32,15 @@
 //               S buffer; rescale O in TMEM only when the running max grows by
 //               more than 2^8, so rescales are rare; final normalisation and
 //               bf16 store.
-// 8-bit slabs (int8 or fp8 per-token-head codes): the producers dequantise
-// the prefix rows (code * scale, rounded to bf16) into the same shared-memory
-// layout instead of copying them; the chunk rows are bf16 either way.
+// 8-bit slabs (int8 or fp8 per-token-head codes): every MMA operand is f16.
+// The producers dequantise the prefix rows (code * scale, rounded once to f16)
+// into the same shared-memory layout instead of copying them, and convert the
+// bf16 chunk rows to f16; the softmax warps write Q as f16.  A value f16
+// cannot hold (magnitude 65520 or more) saturates to +-65504 and sets
+// FA_DEV_ERR_RANGE.
 // Every wait is bounded; tensor memory is always freed.
 #include <cfloat>
+#include <cstdlib>
 
 #include <cuda_fp8.h>
 
@@ -117,12 +121,13 @@ struct ExtK {
 };
 
 // The key tiles one CTA walks: prefix tiles (16-aligned starts, from the
-// slab) then chunk tiles (64-aligned relative to P, from k_ext / v_ext).
+// slab) then chunk tiles (tile-aligned relative to P, from k_ext / v_ext).
 // The CTAs of one (sequence, KV head) read the same prefix tiles; each walks
 // them from a different starting tile (rot), so at any moment they read
 // different lines and the L2 slices share the load.  The softmax does not
 // depend on the order of the tiles.
 struct ExtPlan {
+  int nk;                  // keys per tile (64 or 128)
   int b, h, ds, t0, n, P, qo0;
   int Pk;                  // keys [0, Pk) come from the slab (P, or all keys when keys_in_pages)
   int kmin, kmax;          // visible key positions of the CTA's rows
@@ -135,13 +140,15 @@ struct ExtPlan {
     if (j < np) {
       int k = j + rot;
       if (k >= np) k -= np;
-      return a0 + 64 * k;
+      return a0 + nk * k;
     }
-    return c0 + 64 * (j - np);
+    return c0 + nk * (j - np);
   }
 };
 
+template <int NK>
 __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
+  x.nk = NK;
   x.b = blockIdx.z;
   x.h = blockIdx.y / p.dslices;
   x.ds = blockIdx.y % p.dslices;
@@ -173,25 +180,19 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   x.kmax = q_last;
   x.np = 0;
   x.a0 = (x.kmin / 16) * 16;
-  if (x.kmin < x.Pk) x.np = (x.Pk - x.a0 + 63) / 64;
+  if (x.kmin < x.Pk) x.np = (x.Pk - x.a0 + NK - 1) / NK;
   const int cfirst = max(x.kmin, x.Pk);
-  x.c0 = x.Pk + ((cfirst - x.Pk) / 64) * 64;
-  x.nc = (x.kmax >= x.c0) ? (x.kmax - x.c0) / 64 + 1 : 0;
+  x.c0 = x.Pk + ((cfirst - x.Pk) / NK) * NK;
+  x.nc = (x.kmax >= x.c0) ? (x.kmax - x.c0) / NK + 1 : 0;
   x.rot = x.np > 1 ? static_cast<int>((blockIdx.x * 2u + x.ds) * 5u % static_cast<unsigned>(x.np)) : 0;
   return true;
 }
 
-// f16 pair of two fp32 values, magnitudes above the f16 range saturating.
-__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-  return pack_f16x2(fminf(fmaxf(lo, -65504.f), 65504.f), fminf(fmaxf(hi, -65504.f), 65504.f));
-}
-
 // 32 consecutive 8-bit codes (two 16-byte words) times the row's scale,
-// rounded once and packed in pairs: bf16 for K (the S MMA's operand, Q being
-// bf16), f16 for V (the PV MMA runs in f16 for 8-bit slabs, P being f16, so
-// the dequantised V keeps three more mantissa bits).  int8 codes are exact in
-// fp32, e4m3 codes exact in f16.
-template <int KV, bool F16>
+// rounded once to f16 and packed in pairs (the MMAs over 8-bit slabs run in
+// f16, which keeps 11 significant bits of the dequantised values).  int8 codes
+// are exact in fp32, e4m3 codes exact in f16.
+template <int KV>
 __device__ __forceinline__ void dequant32(const uint4 (&w)[2], float s, uint32_t (&out)[16]) {
   const uint32_t word[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
@@ -212,23 +213,48 @@ __device__ __forceinline__ void dequant32(const uint4 (&w)[2], float s, uint32_t
         f[2 * b + 1] = ff.y;
       }
     }
-    if constexpr (F16) {
-      out[2 * i] = pack_f16x2_sat(f[0] * s, f[1] * s);
-      out[2 * i + 1] = pack_f16x2_sat(f[2] * s, f[3] * s);
-    } else {
-      out[2 * i] = pack_bf16x2(f[0] * s, f[1] * s);
-      out[2 * i + 1] = pack_bf16x2(f[2] * s, f[3] * s);
-    }
+    out[2 * i] = pack_f16x2_sat(f[0] * s, f[1] * s);
+    out[2 * i + 1] = pack_f16x2_sat(f[2] * s, f[3] * s);
   }
 }
 
-// 32 consecutive bf16 values (four 16-byte words) as f16 pairs (saturating).
-__device__ __forceinline__ void bf16_to_f16_32(const uint4 (&w)[4], uint32_t (&out)[16]) {
+// A row of 8-bit codes with this scale dequantises to a value f16 cannot hold:
+// its largest code magnitude (127 for int8, 448 for e4m3) times the scale
+// reaches 65520, where f16 rounding would give infinity.
+template <int KV>
+__device__ __forceinline__ bool scale_past_f16(float s) {
+  return fabsf(s) * (KV == FA_KV_INT8 ? 127.0f : 448.0f) >= 65520.0f;
+}
+
+// 32 consecutive bf16 values (four 16-byte words) as f16 pairs (saturating);
+// returns nonzero if any of them lies past the f16 range.
+__device__ __forceinline__ uint32_t bf16_to_f16_32(const uint4 (&w)[4], uint32_t (&out)[16]) {
   const uint32_t word[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
                              w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
+  uint32_t big = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) out[i] = pack_f16x2_sat(__uint_as_float(word[i] << 16), __uint_as_float(word[i] & 0xffff0000u));
+  for (int i = 0; i < 16; ++i) {
+    big |= bf16x2_past_f16(word[i]);
+    out[i] = pack_f16x2_sat(__uint_as_float(word[i] << 16), __uint_as_float(word[i] & 0xffff0000u));
+  }
+  return big;
 }
+
+// The two softmax warps of a row (each holding half of a tile's scores)
+// must compute their weights against one common base at least the row's
+// largest scaled score.  Each publishes its half's maximum rounded up to an
+// integer (log2 units) as an int16, so the common base max(a, b) exceeds the
+// true maximum by less than 1 and the largest weight stays in (0.5, 1] (a
+// rounding to bf16 would leave up to |max| / 256 of excess, which makes f16
+// weights underflow once scores reach a few thousand).  INT16_MIN stands for
+// "no visible key"; a maximum past +-32767 saturates and is reported.
+__device__ __forceinline__ short max_code(float m, bool& out_of_range) {
+  if (m == -INFINITY) return static_cast<short>(-32768);
+  const float c = ceilf(m);
+  out_of_range |= !(c <= 32767.f && c >= -32767.f);
+  return static_cast<short>(fminf(fmaxf(c, -32767.f), 32767.f));
+}
+__device__ __forceinline__ float max_decode(short c) { return c == -32768 ? -INFINITY : static_cast<float>(c); }
 
 template <int D, int KV>
 __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
@@ -254,7 +280,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   if (!p.early_metadata) griddep_wait();
   griddep_launch_dependents();
   ExtPlan x;
-  if (!ext_plan(p, x)) return;
+  if (!ext_plan<64>(p, x)) return;
   const int nt = x.tiles();
 
   if (threadIdx.x == 0) {
@@ -386,13 +412,15 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
               const float* scl = is_v ? p.v_scale : p.k_scale;
               const int rr = lane >> 1, cpart = lane & 1;
               float s4[4];
-              bool v4[4];
+              bool v4[4], big = false;
 #pragma unroll
               for (int g = 0; g < 4; ++g) {
                 const int r = 16 * g + rr;
                 v4[g] = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
                 s4[g] = v4[g] ? __ldg(scl + (v4[g] ? ts.row0[g] + rr : 0)) : 0.f;
+                big |= scale_past_f16<KV>(s4[g]);
               }
+              if (__any_sync(0xffffffffu, big) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
 #pragma unroll 1
               for (int h = 0; h < C::CPS; ++h) {
 #pragma unroll
@@ -403,7 +431,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
                   w[0] = v4[g] ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
                   w[1] = v4[g] ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
                   uint32_t pk[16];
-                  dequant32<KV, true>(w, s4[g], pk);
+                  dequant32<KV>(w, s4[g], pk);
 #pragma unroll
                   for (int u = 0; u < 4; ++u)
                     *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(16 * g + rr, cpart * 4 + u)) =
@@ -420,6 +448,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
               // chunk read as zero
               const uint8_t* ext = is_v ? p.v_ext : p.k_ext;
               const int rr = lane >> 1, cpart = lane & 1;
+              uint32_t big = 0;
 #pragma unroll 1
               for (int h = 0; h < C::CPS; ++h) {
 #pragma unroll
@@ -433,13 +462,14 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
 #pragma unroll
                   for (int i = 0; i < 4; ++i) w[i] = v ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
                   uint32_t pk[16];
-                  bf16_to_f16_32(w, pk);
+                  big |= bf16_to_f16_32(w, pk);
 #pragma unroll
                   for (int u = 0; u < 4; ++u)
                     *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(r, cpart * 4 + u)) =
                         make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
               }
+              if (__any_sync(0xffffffffu, big != 0) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
               fence_proxy_async_smem();
               if (lane == 0) mbar_arrive_expect_tx(&full[sl], 0);
               mbar_arrive(&full[sl]);
@@ -612,15 +642,16 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     // the first four take columns [0, 32) of each 64-key tile, the other four
     // columns [32, 64).  The two halves of a row exchange their tile maxima
     // through shared memory (double buffered by tile parity) once per tile,
-    // each rounded up to bf16 so that both halves take the same value (any
-    // common base gives the same softmax); that barrier ANDs each warp's wait
+    // each rounded up to an integer so that both halves take the same value
+    // (any common base gives the same softmax); that barrier ANDs each warp's wait
     // result, so all eight leave the loop together.  Each half keeps its share
     // of the denominator; the shares meet once in the epilogue, through the
     // ring, which is idle by then.
-    __shared__ __nv_bfloat16 sm_mx[2][2][C::M];   // [tile parity][half][row]
+    __shared__ short sm_mx[2][2][C::M];   // [tile parity][half][row]: max_code values
     constexpr int SMX_BAR = 2, SMX_THREADS = C::NSMX * 32;
     const int half = (warp - (C::W_MMA + 1)) >> 2;
     const int quarter = warp & 3;
+    bool range_bad = false;
     const int r = quarter * 32 + lane;   // query row = tensor-memory lane
     const int tl = r / p.g, hj = r % p.g;
     const int t = x.t0 + tl;
@@ -638,6 +669,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       const bool in = tok < p.num_tokens;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
       constexpr int QBLK = KV == FA_KV_BF16 ? C::NQT : C::KB;
+      uint32_t qbig = 0;
 #pragma unroll 1
       for (int kb = half; kb < QBLK; kb += 2) {
         uint32_t w[32];
@@ -651,7 +683,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         }
         if constexpr (KV != FA_KV_BF16) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = pack_f16x2_sat(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+          for (int i = 0; i < 32; ++i) {
+            qbig |= bf16x2_past_f16(w[i]);
+            w[i] = pack_f16x2_sat(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+          }
         }
         if (kb < C::NQT) {
           tmem_st32(trow + C::Q_COL0 + kb * 32, w);
@@ -662,7 +697,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
             *reinterpret_cast<uint4*>(qb + sw128(r, u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      if constexpr (KV != FA_KV_BF16) fence_proxy_async_smem();   // the Q rows written here, for the S MMA
+      if constexpr (KV != FA_KV_BF16) {
+        fence_proxy_async_smem();   // the Q rows written here, for the S MMA
+        if (__any_sync(0xffffffffu, qbig != 0) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -670,7 +708,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     }
     const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
     const float sc = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;   // l_run: this half's share of the denominator
+    // l_run: this half's share of the denominator, the sum of the rounded
+    // weights the PV MMA uses (so constant V gives exactly that constant);
+    // l_lse: the same sum of the unrounded weights, for lse
+    float m_run = -INFINITY, l_run = 0.f, l_lse = 0.f;
     bool ok = true, bad = false;
     constexpr int OH = C::DS / 2;            // O columns this half rescales and writes
     for (int j = 0; j < nt; ++j) {
@@ -701,15 +742,15 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
 #pragma unroll
         for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
-        const __nv_bfloat16 mr = __float2bfloat16_ru(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc);
+        const short mr = max_code(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc, range_bad);
         sm_mx[sb][half][r] = mr;
-        mt = __bfloat162float(mr);
+        mt = max_decode(mr);
       }
       // every warp has loaded its S half (so P may now overwrite the S
       // buffer) and published its maximum
       ok = named_bar_and(SMX_BAR, SMX_THREADS, got && !bad);
       if (!ok) break;
-      mt = fmaxf(mt, __bfloat162float(sm_mx[sb][half ^ 1][r]));
+      mt = fmaxf(mt, max_decode(sm_mx[sb][half ^ 1][r]));
       const float m_new = fmaxf(m_run, mt);
       const bool need = m_new > m_run + 8.0f;   // rescale only when the max grows by more than 2^8
       if (__any_sync(0xffffffffu, need && m_run > -INFINITY) && j > 0) {
@@ -733,17 +774,20 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         }
       }
       if (need) {
-        l_run = (m_run > -INFINITY) ? l_run * ex2(m_run - m_new) : 0.f;
+        const float f = (m_run > -INFINITY) ? ex2(m_run - m_new) : 0.f;
+        l_run *= f;
+        l_lse *= f;
         m_run = m_new;
       }
       uint32_t pk[16];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      float ps[4] = {0.f, 0.f, 0.f, 0.f}, pe[2] = {0.f, 0.f};
       // a row with no visible key so far has m_run = -inf and only -inf scores: exponent base 0 gives 0
       const float mb = (m_run > -INFINITY) ? m_run : 0.f;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
         const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
+        pe[c & 1] += p0 + p1;
         // the denominator sums the rounded weights the PV MMA uses (bf16, or
         // f16 for 8-bit slabs)
         if constexpr (KV == FA_KV_BF16) {
@@ -756,6 +800,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         }
       }
       l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      l_lse += pe[0] + pe[1];
       tmem_st16(trow + s_col + 16 * half, pk);   // P of keys [32 half, 32 half + 32): 16 columns of bf16 pairs
       tmem_st_wait();
       tc_fence_before();
@@ -763,13 +808,18 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       if (lane == 0) mbar_arrive(&p_full[sb]);
     }
     // ------------------------------------------------------------ epilogue
+    if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
     bool fin = ok;
     if (fin && nt > 0) fin = __all_sync(0xffffffffu, mbar_wait(&o_bar[(nt - 1) & 1], ((nt - 1) >> 1) & 1));
     // every MMA has completed, so every ring slot was consumed: the ring is idle
-    float* sm_l = reinterpret_cast<float*>(ring);   // [half][row]
-    if (fin) sm_l[half * C::M + r] = l_run;
+    float* sm_l = reinterpret_cast<float*>(ring);   // [half][row]: rounded sums, then unrounded ones
+    if (fin) {
+      sm_l[half * C::M + r] = l_run;
+      sm_l[(2 + half) * C::M + r] = l_lse;
+    }
     fin = named_bar_and(SMX_BAR, SMX_THREADS, fin);
     const float l_tot = fin ? l_run + sm_l[(half ^ 1) * C::M + r] : 0.f;
+    const float l_all = fin ? l_lse + sm_l[(2 + (half ^ 1)) * C::M + r] : 0.f;
     if (!fin) {
       if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     } else {
@@ -794,7 +844,553 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       }
       if (row_ok && half == 0 && x.ds == 0 && p.lse)
         p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
-            (m_run > -INFINITY && l_tot > 0.f) ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+            (m_run > -INFINITY && l_all > 0.f) ? (m_run + __log2f(l_all)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 slabs: 128-key tiles.
+//
+// An M = 128 tcgen05.mma costs about the same at N = 64 as at N = 128 (the
+// instruction rate, not the tensor pipe, bounds N = 64), so S = Q K^T over
+// 128 keys per tile takes half the MMAs of the 64-key kernel above, and PV
+// runs as one N = 256 MMA per 16 keys over the CTA's whole output slice.
+// Tensor memory (512 columns): O [0, 256), S [256, 384) (fp32, 128 keys),
+// and Q's first 256 columns as bf16 pairs [384, 512); Q's other 256 columns
+// (head_dim 512) stay in shared memory.  S has one buffer, released as soon
+// as the softmax warps hold it in registers, so S of the next tile runs while
+// they work.  P (bf16) goes to shared memory as the A operand of the PV MMA
+// (two 64-key blocks in the 128-byte-swizzled K-major layout), written once
+// the previous PV has read it.
+// The K/V ring holds 16 KB chunks (128 keys x 64 columns); a tile's K passes
+// as KB chunks, its V slice as 4 chunks in 4 consecutive slots, so the ring
+// length (a multiple of 4) never splits the V group the N = 256 MMA spans.
+// Roles as above: warps 0-3 fill ring slot e (warp e % 4), TMA for page
+// groups 0-3 of a prefix chunk and cp.async for groups 4-7; warp 4 issues the
+// MMAs; warps 5-12 run the softmax, two per tensor-memory lane quarter, each
+// thread one query row and 64 of a tile's 128 columns.
+template <int D>
+struct E128Cfg {
+  static constexpr int M = 128;                  // query rows per CTA
+  static constexpr int NK = 128;                 // keys per tile
+  static constexpr int NGRP = NK / 16;           // 16-row page groups per tile
+  static constexpr int DS = 256;                 // output columns per CTA
+  static constexpr int NVB = DS / 64;            // V chunks per tile
+  static constexpr int KB = D / 64;              // K chunks per tile (64 columns each)
+  static constexpr int NQT = 4;                  // Q blocks in tensor memory
+  static constexpr int NQS = KB - NQT;           // Q blocks in shared memory
+  static constexpr int CHUNK = NK * 128;         // 128 keys x 64 columns bf16
+  static constexpr int Q_BYTES = NQS * M * 128;  // [NQS][128 rows][128 B]
+  static constexpr int P_BYTES = 2 * M * 128;    // [2 key blocks][128 rows][128 B]
+  static constexpr int BAR_BYTES = 1024;
+  // dynamic shared memory: the opt-in maximum less the static array below
+  // (1 KB) and the 1 KB alignment slack
+  static constexpr int AVAIL = 232448 - 1024 - 1024;
+  static constexpr int NSLOT = (AVAIL - Q_BYTES - P_BYTES - BAR_BYTES) / CHUNK / 4 * 4;
+  static constexpr int OFF_P = Q_BYTES;
+  static constexpr int OFF_RING = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * CHUNK;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM_ALLOC = SMEM + 1024;
+  static constexpr int TMA_GROUPS = NGRP / 2;   // page groups by TMA, the rest by cp.async
+  static constexpr int NPW = 4;                 // producer warps
+  static constexpr int W_MMA = NPW;
+  static constexpr int NSMX = 8;                // softmax warps
+  static constexpr int NTHR = (NPW + 1 + NSMX) * 32;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL0 = DS;
+  static constexpr uint32_t Q_COL0 = DS + NK;
+  static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
+  static_assert(KB % 4 == 0 && NVB == 4, "a tile's K and V chunks come in groups of 4");
+  static_assert(NSLOT % 4 == 0 && NSLOT >= 8, "ring of whole V groups");
+  static_assert(NPW <= NSLOT, "producer stride within one ring lap");
+  static_assert(SMEM_ALLOC + 1024 <= 232448, "shared memory budget");
+  static_assert((1 + 2 * NSLOT + 6) * 8 + 8 <= BAR_BYTES, "barrier space");
+  static_assert(OFF_P % 1024 == 0 && OFF_RING % 1024 == 0 && CHUNK % 1024 == 0, "swizzle atoms");
+};
+
+template <int D>
+__global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
+    extend128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kx,
+                     const __grid_constant__ CUtensorMap tm_vx, const ExtK p) {
+  using C = E128Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem;
+  uint8_t* ps = smem + C::OFF_P;
+  uint8_t* ring = smem + C::OFF_RING;
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = q_full + 1;          // [NSLOT]
+  uint64_t* empty = full + C::NSLOT;    // [NSLOT]
+  uint64_t* s_full = empty + C::NSLOT;  // S_t is in tensor memory
+  uint64_t* s_free = s_full + 1;        // every softmax warp holds S_t in registers
+  uint64_t* p_full = s_free + 1;        // P_t is in shared memory
+  uint64_t* o_bar = p_full + 1;         // PV_t has completed
+  uint64_t* qt_full = o_bar + 1;        // the softmax warps have put Q into tensor memory
+  uint64_t& done_bar = qt_full[1];      // every MMA has completed (before tensor memory is freed)
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(qt_full + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!p.early_metadata) griddep_wait();
+  griddep_launch_dependents();
+  ExtPlan x;
+  if (!ext_plan<C::NK>(p, x)) return;
+  const int nt = x.tiles();
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(&full[i], 33);   // the filling warp: lane 0's expect_tx + 32 lane arrivals
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, C::NSMX);
+    mbar_init(p_full, C::NSMX);
+    mbar_init(o_bar, 1);
+    mbar_init(qt_full, C::NSMX);
+    mbar_init(&done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == C::W_MMA) tmem_alloc(&tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  griddep_wait();   // from here on q, k, v, the slab and the outputs are touched
+
+  if (warp < C::NPW) {
+    // ----------------------------------------------------------- producers
+    // Emission order = the MMA issuer's consumption order: K_0, then for each
+    // t >= 1: K_t (if any) and V_{t-1}; slot e by warp e % NPW.  A prefix
+    // chunk is 8 page groups of 16 rows: groups 0-3 by TMA (one 2 KB box per
+    // group), groups 4-7 by the warp's cp.async copies; a group without a
+    // page, past the prefix end, before the window start or holding the
+    // prefix end goes by cp.async with zero fill (its stale rows, NaN
+    // included, must not reach the MMAs).  A chunk of k_ext / v_ext rows is
+    // two 64-row boxes.  full[] counts 33 arrivals: lane 0's expect_tx, then
+    // 32 lane arrivals (when their cp.async copies land, or at once).
+    const int pw = warp;
+    const uint64_t pol = l2_policy_evict_last();   // K/V rows are shared by the CTAs of a (sequence, head)
+    if (threadIdx.x == 0) {
+      prefetch_tmap(&tm_q);
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int kb = C::NQT; kb < C::KB; ++kb)
+        tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
+    }
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_kx);
+      prefetch_tmap(&tm_vx);
+    }
+    const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
+    struct PageRef {
+      int pid, off;
+    };
+    // page of row group `lane` (lanes 0-7) of tile j and the group's offset
+    // in it, looked up a tile ahead; the id is checked where it is used
+    auto load_pid = [&](int j) -> PageRef {
+      PageRef r{-1, 0};
+      if (j < nt && x.prefix(j) && lane < C::NGRP) {
+        const int pos = x.start(j) + 16 * lane;   // a 16-row group lies in one page
+        if (pos < x.Pk) {
+          const int q = pos / p.page_size;
+          r.off = pos - q * p.page_size;
+          r.pid = ld_nc_early(bt + q);
+        }
+      }
+      return r;
+    };
+    struct TileSrc {
+      int row0[C::NGRP];   // slab row of each 16-row group (prefix tiles), -1: no page
+      int lim;             // rows [0, lim) of the tile hold keys
+      int wlim;            // rows below wlim precede every visible key of the CTA: read as zero
+      int bgroup;          // the group holding the prefix end inside it, -1: none
+      bool prefix;
+      int tok0;            // chunk tiles: first token row in k_ext / v_ext
+    };
+    auto tile_src = [&](int j, PageRef pr) {
+      TileSrc ts;
+      const int st0 = x.start(j);
+      ts.prefix = x.prefix(j);
+      ts.lim = ts.prefix ? x.Pk - st0 : x.n - (st0 - x.P);
+      ts.bgroup = (ts.prefix && ts.lim < C::NK && (ts.lim & 15) != 0) ? (ts.lim >> 4) : -1;
+      ts.tok0 = x.qo0 + st0 - x.P;
+      ts.wlim = ts.prefix ? max(0, x.kmin - st0) : 0;
+      int r0 = -1;
+      if (lane < C::NGRP && ts.prefix && 16 * lane < ts.lim) {
+        if (pr.pid < 0 || pr.pid >= p.num_pages) {
+          if (pw == 0) atomicOr(p.err, FA_DEV_ERR_PAGE);
+        } else {
+          r0 = (pr.pid * p.Hkv + x.h) * p.page_size + pr.off;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < C::NGRP; ++g) ts.row0[g] = __shfl_sync(0xffffffffu, r0, g);
+      return ts;
+    };
+    auto by_tma = [&](const TileSrc& ts, int g) {
+      return g < C::TMA_GROUPS && g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
+    };
+    int e = 0;
+    bool ok = true;
+    // one slot: column block blk (64 columns) of the tile's K or V rows
+    auto emit = [&](const TileSrc& ts, int blk, bool is_v) {
+      if (e % C::NPW == pw) {
+        const int sl = e % C::NSLOT;
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+        ok = __shfl_sync(0xffffffffu, w, 0) && ok;
+        if (ok) {
+          uint8_t* dst = ring + sl * C::CHUNK;
+          if (ts.prefix) {
+            if (lane == 0) {
+              int tx = 0;
+#pragma unroll
+              for (int g = 0; g < C::NGRP; ++g)
+                if (by_tma(ts, g)) tx += 2048;
+              mbar_arrive_expect_tx(&full[sl], tx);
+#pragma unroll
+              for (int g = 0; g < C::NGRP; ++g)
+                if (by_tma(ts, g))
+                  tma_load_3d(dst + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk, ts.row0[g], pol);
+            }
+            const uint8_t* base = is_v ? p.v_slab : p.k_slab;
+            bool any_cp = false;
+#pragma unroll
+            for (int g = 0; g < C::NGRP; ++g) {
+              if (by_tma(ts, g)) continue;
+              any_cp = true;
+              // 16 rows x 8 units: lane copies rows lane / 8 + 4 i, unit lane % 8
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
+                const bool v = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
+                const uint8_t* src =
+                    base + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + blk * 64) * 2 + (lane & 7) * 16 : 0);
+                cp_async16_zfill(dst + sw128(r, lane & 7), src, v, pol);
+              }
+            }
+            if (any_cp) cp_async_mbar_arrive(&full[sl]);
+            else if (lane == 0) mbar_arrive_n(&full[sl], 32);
+          } else {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&full[sl], C::CHUNK);
+              tma_load_4d(dst, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, ts.tok0, pol);
+              tma_load_4d(dst + C::CHUNK / 2, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, ts.tok0 + 64, pol);
+              mbar_arrive_n(&full[sl], 32);
+            }
+          }
+        }
+      }
+      ++e;
+    };
+    PageRef pid_next = load_pid(0);
+    TileSrc src_cur{}, src_prev{};
+    for (int t = 0; ok && t <= nt; ++t) {
+      if (t < nt) {
+        const PageRef pid = pid_next;
+        pid_next = load_pid(t + 1);   // a tile ahead
+        src_cur = tile_src(t, pid);
+        for (int kb = 0; ok && kb < C::KB; ++kb) emit(src_cur, kb, false);
+      }
+      if (t >= 1)
+        for (int i = 0; ok && i < C::NVB; ++i) emit(src_prev, x.ds * C::NVB + i, true);
+      src_prev = src_cur;
+    }
+    if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    // drain: no copy may still be landing when the CTA exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (lane == 0) {
+      for (int i = max(0, e - C::NSLOT); i < e; ++i)
+        if (i % C::NPW == pw && !mbar_wait(&full[i % C::NSLOT], (i / C::NSLOT) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    }
+    if (threadIdx.x == 0 && !mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+  } else if (warp == C::W_MMA) {
+    // ---------------------------------------------------------- MMA issuer
+    // The whole warp walks the schedule and waits on the barriers; one
+    // elected lane issues the MMAs and the commits that track them.
+    const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);   // S: N = 128 keys, K-major B
+    const uint32_t idO = umma_idesc_bf16(C::M, C::DS, true);    // PV: N = 256 columns, MN-major B
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0) && mbar_wait(qt_full, 0));
+    tc_fence_after();
+    const uint64_t qd0 = umma_desc_sw128(smem_u32(qs), 16, 1024);   // Q's shared-memory blocks
+    const uint64_t pd0 = umma_desc_sw128(smem_u32(ps), 16, 1024);   // P's two key blocks
+    const uint32_t s_tmem = tmem + C::S_COL0;
+    int e = 0;
+    auto wait_slot = [&](int ee) -> uint32_t {   // wait for ring position ee, return its address
+      const int sl = ee % C::NSLOT;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[sl], (ee / C::NSLOT) & 1));
+      return smem_u32(ring + sl * C::CHUNK);
+    };
+    for (int t = 0; ok && t <= nt; ++t) {
+      if (t < nt) {
+        // S_t overwrites S once every softmax warp holds S_{t-1} in registers
+        if (t >= 1) ok = __all_sync(0xffffffffu, mbar_wait(s_free, (t - 1) & 1));
+        tc_fence_after();
+        for (int kb = 0; ok && kb < C::KB; ++kb) {
+          const uint32_t kaddr = wait_slot(e);
+          if (!ok) break;
+          fence_proxy_async_smem();   // the cp.async writes, seen through the barrier, for the MMA's reads
+          tc_fence_after();
+          // one descriptor per chunk; a K16 step advances 32 bytes along the
+          // swizzled row (start-address field +2, no carry below 256 KB)
+          const uint64_t kd = umma_desc_sw128(kaddr, 16, 1024);
+          if (elect_one()) {
+            if (kb < C::NQT) {   // A = Q block from tensor memory
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, kd + 2 * ks, idS, (kb > 0 || ks > 0) ? 1u : 0u);
+            } else {             // A = Q block from shared memory
+              const uint64_t qd = qd0 + static_cast<uint64_t>((kb - C::NQT) * (C::M * 128) / 16);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) umma_ss(s_tmem, qd + 2 * ks, kd + 2 * ks, idS, 1u);
+            }
+            umma_commit(&empty[e % C::NSLOT]);   // the chunk is free once these MMAs complete
+          }
+          __syncwarp();
+          ++e;
+        }
+        if (!ok) break;
+        if (elect_one()) umma_commit(s_full);   // S_t completes phase t of s_full
+        __syncwarp();
+      }
+      if (t >= 1) {
+        const int i = t - 1;
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(p_full, i & 1));   // P_i is in shared memory
+        if (!ok) break;
+        // V_i: NVB chunks in consecutive slots (a group never wraps the ring)
+        uint32_t vaddr = 0;
+        for (int v = 0; ok && v < C::NVB; ++v) {
+          const uint32_t a = wait_slot(e + v);
+          if (v == 0) vaddr = a;
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint64_t vd0 = umma_desc_sw128(vaddr, C::CHUNK, 1024);   // LBO: chunk stride along N
+        if (elect_one()) {
+#pragma unroll
+          for (int ks = 0; ks < C::NK / 16; ++ks)
+            umma_ss(tmem, pd0 + static_cast<uint64_t>((ks >> 2) * (C::M * 128) / 16 + 2 * (ks & 3)),
+                    vd0 + static_cast<uint64_t>(ks * 2048 / 16), idO, (i > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int v = 0; v < C::NVB; ++v) umma_commit(&empty[(e + v) % C::NSLOT]);
+          umma_commit(o_bar);   // PV_i completes phase i of o_bar
+        }
+        __syncwarp();
+        e += C::NVB;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    // every MMA the elected lane issued has finished before tensor memory is freed
+    if (elect_one()) umma_commit(&done_bar);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(&done_bar, 0)) && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+  } else {
+    // ------------------------------------------------------------- softmax
+    // Two warps per row quarter (tensor-memory lane access follows warp % 4):
+    // the first four take columns [0, 64) of each 128-key tile, the other
+    // four [64, 128).  They exchange their tile maxima through shared memory
+    // (rounded up to integers, max_code), keep their own
+    // shares of the denominator, and meet once in the epilogue.
+    __shared__ short sm_mx[2][2][C::M];   // [tile parity][half][row]: max_code values
+    constexpr int SMX_BAR = 2, SMX_THREADS = C::NSMX * 32;
+    constexpr int HC = C::NK / 2;                // score columns per thread
+    bool range_bad = false;
+    const int half = (warp - (C::W_MMA + 1)) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;   // query row = tensor-memory lane
+    const int tl = r / p.g, hj = r % p.g;
+    const int t = x.t0 + tl;
+    const bool row_ok = t < x.n;
+    const int qpos = x.P + t;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    {
+      // this row's first NQT * 64 query values into tensor memory (row =
+      // lane, bf16 pairs per column: the A-operand layout of the S MMA),
+      // half h copying blocks h, h + 2; rows past the last token are zero
+      const int tok = x.qo0 + t;
+      const bool in = tok < p.num_tokens;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
+#pragma unroll 1
+      for (int kb = half; kb < C::NQT; kb += 2) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = in ? __ldg(src + kb * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        tmem_st32(trow + C::Q_COL0 + kb * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qt_full);
+    }
+    const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
+    const float sc = p.scale_log2;
+    // l_run: this half's share of the denominator, the sum of the bf16
+    // weights the PV MMA uses; l_lse: the sum of the unrounded weights, for lse
+    float m_run = -INFINITY, l_run = 0.f, l_lse = 0.f;
+    bool ok = true, bad = false;
+    constexpr int OH = C::DS / 2;            // O columns this half rescales and writes
+    uint8_t* prow = ps + half * (C::M * 128);   // this half's P block: keys [64 half, 64 half + 64)
+    for (int j = 0; j < nt; ++j) {
+      const int xb = j & 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1));
+      const bool pre = x.prefix(j);
+      const int st0 = x.start(j) + HC * half;   // key of this half's first column
+      float sv[HC];
+      float mt = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        uint32_t sa[32], sb[32];
+        tmem_ld32(trow + C::S_COL0 + HC * half, sa);
+        tmem_ld32(trow + C::S_COL0 + HC * half + 32, sb);
+        tmem_ld_wait();
+        // this warp's part of S_j is in registers: S may take S_{j+1}
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.Pk - 1) : qpos);
+        const int clo = klo - st0, chi = khi - st0;
+        if (__all_sync(0xffffffffu, clo <= 0 && chi >= HC - 1)) {   // every column visible to the warp's rows
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            sv[c] = __uint_as_float(sa[c]);
+            sv[32 + c] = __uint_as_float(sb[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sa[c]) : -INFINITY;
+            sv[32 + c] = (32 + c >= clo && 32 + c <= chi) ? __uint_as_float(sb[c]) : -INFINITY;
+          }
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
+#pragma unroll
+        for (int c = 0; c < HC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+        const short mr = max_code(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc, range_bad);
+        sm_mx[xb][half][r] = mr;
+        mt = max_decode(mr);
+      }
+      // every warp has published its maximum
+      ok = named_bar_and(SMX_BAR, SMX_THREADS, got && !bad);
+      if (!ok) break;
+      mt = fmaxf(mt, max_decode(sm_mx[xb][half ^ 1][r]));
+      const float m_new = fmaxf(m_run, mt);
+      const bool need = m_new > m_run + 8.0f;   // rescale only when the max grows by more than 2^8
+      const bool resc = need && m_run > -INFINITY;
+      const float f = resc ? ex2(m_run - m_new) : (need ? 0.f : 1.0f);   // this row's factor for O and l
+      if (need) {
+        l_run *= f;
+        l_lse *= f;
+        m_run = m_new;
+      }
+      // the weights first, in registers: only their store and the rescale of O
+      // wait for PV_{j-1}
+      // a row with no visible key so far has m_run = -inf and only -inf scores: exponent base 0 gives 0
+      const float mb = (m_run > -INFINITY) ? m_run : 0.f;
+      float lsum[4] = {0.f, 0.f, 0.f, 0.f}, pe[2] = {0.f, 0.f};
+      uint32_t pk[HC / 2];
+#pragma unroll
+      for (int c = 0; c < HC / 2; ++c) {
+        const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
+        const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
+        pe[c & 1] += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+        // the denominator sums the bf16-rounded weights the PV MMA uses
+        lsum[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+      }
+      // PV_{j-1} must have completed before O is rescaled and before P_j
+      // overwrites the P that PV_{j-1} reads
+      bool pv_done = true;
+      if (j > 0) {
+        pv_done = __all_sync(0xffffffffu, mbar_wait(o_bar, (j - 1) & 1));
+        if (!pv_done) {
+          bad = true;   // leaves the loop at the next tile's barrier
+          if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+        }
+      }
+      if (pv_done && __any_sync(0xffffffffu, resc) && j > 0) {
+        tc_fence_after();
+        const float fo = resc ? f : 1.0f;
+        // 16 columns at a time: the weights of this tile are live in registers
+#pragma unroll 1
+        for (int c = half * OH; c < (half + 1) * OH; c += 16) {
+          uint32_t o[16];
+          tmem_ld16(trow + c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * fo);
+          tmem_st16(trow + c, o);
+        }
+        tmem_st_wait();
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)   // 8 keys per 16-byte unit of the P row
+        *reinterpret_cast<uint4*>(prow + sw128(r, u)) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      l_run += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+      l_lse += pe[0] + pe[1];
+      // the generic P writes, ordered for the PV MMA's async-proxy reads
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
+    bool fin = ok;
+    if (fin && nt > 0) fin = __all_sync(0xffffffffu, mbar_wait(o_bar, (nt - 1) & 1));
+    // every MMA has completed, so every ring slot was consumed: the ring is idle
+    float* sm_l = reinterpret_cast<float*>(ring);   // [half][row]: rounded sums, then unrounded ones
+    if (fin) {
+      sm_l[half * C::M + r] = l_run;
+      sm_l[(2 + half) * C::M + r] = l_lse;
+    }
+    fin = named_bar_and(SMX_BAR, SMX_THREADS, fin);
+    const float l_tot = fin ? l_run + sm_l[(half ^ 1) * C::M + r] : 0.f;
+    const float l_all = fin ? l_lse + sm_l[(2 + (half ^ 1)) * C::M + r] : 0.f;
+    if (!fin) {
+      if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const float inv = (l_tot > 0.f) ? 1.0f / l_tot : 0.f;
+      __nv_bfloat16* orow =
+          p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS;
+#pragma unroll 1
+      for (int c = half * OH; c < (half + 1) * OH; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(trow + c, o);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            reinterpret_cast<uint4*>(orow + c)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (row_ok && half == 0 && x.ds == 0 && p.lse)
+        p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
+            (m_run > -INFINITY && l_all > 0.f) ? (m_run + __log2f(l_all)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -816,6 +1412,28 @@ static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStrea
   const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
   return launch_pdl(extend_kernel<D, KV>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
                     a.tm_vx, k);
+}
+
+template <int D>
+static cudaError_t launch_extend128_t(const ExtendArgs& a, const ExtK& k, cudaStream_t s) {
+  using C = E128Cfg<D>;
+  static unsigned int done = 0;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend128_kernel<D>), C::SMEM_ALLOC, &done);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
+  return launch_pdl(extend128_kernel<D>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
+                    a.tm_vx, k);
+}
+
+// bf16 slabs take the 128-key kernel unless FA_EXTEND_TILE=64 selects the
+// 64-key one (both compute the same attention).
+static bool extend_tile64() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("FA_EXTEND_TILE");
+    v = (e && e[0] == '6' && e[1] == '4') ? 1 : 0;
+  }
+  return v == 1;
 }
 
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
@@ -856,7 +1474,9 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
     return a.D == 256 ? launch_extend_t<256, FA_KV_INT8>(a, k, s) : launch_extend_t<512, FA_KV_INT8>(a, k, s);
   if (a.kv_dtype == FA_KV_FP8)
     return a.D == 256 ? launch_extend_t<256, FA_KV_FP8>(a, k, s) : launch_extend_t<512, FA_KV_FP8>(a, k, s);
-  return a.D == 256 ? launch_extend_t<256, FA_KV_BF16>(a, k, s) : launch_extend_t<512, FA_KV_BF16>(a, k, s);
+  if (extend_tile64())
+    return a.D == 256 ? launch_extend_t<256, FA_KV_BF16>(a, k, s) : launch_extend_t<512, FA_KV_BF16>(a, k, s);
+  return a.D == 256 ? launch_extend128_t<256>(a, k, s) : launch_extend128_t<512>(a, k, s);
 }
 
 }  // namespace fa

@@ -52,6 +52,7 @@ struct fa_cache {
   int32_t page_size = 0;
   int32_t kv_dtype = FA_KV_BF16;
   uint32_t flags = 0;   // FA_FLAG_*
+  int32_t err_slot = -1;   // this cache's device error word (index into the per-device array)
 };
 
 namespace fa {
@@ -64,8 +65,10 @@ inline int32_t layer_pages(const fa_cache* c, int32_t layer) {
 // thread-local error message
 fa_status fail(fa_status st, const char* fmt, ...);
 
-// Device error word (one per device, file-scope __device__ storage).
-unsigned int* device_error_word(cudaError_t* err);
+// The cache's device error word on the current device (file-scope
+// __device__ storage, one word per live cache), and its synchronous clear.
+unsigned int* device_error_word(const fa_cache* c, cudaError_t* err);
+cudaError_t clear_device_error_word(const fa_cache* c);
 
 int sm_count();
 

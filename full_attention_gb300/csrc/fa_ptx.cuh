@@ -215,6 +215,20 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// f16 pair of two fp32 values, magnitudes above the f16 range saturating to
+// +-65504 instead of becoming infinite.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  return pack_f16x2(fminf(fmaxf(lo, -65504.f), 65504.f), fminf(fmaxf(hi, -65504.f), 65504.f));
+}
+// Nonzero when either bf16 of the pair (low and high 16 bits of w) has a
+// magnitude of 65536 or more, infinities and NaN included: the bf16 values
+// that f16 cannot hold (f16 ends at 65504; bf16 steps from 65280 to 65536).
+// Each 15-bit magnitude plus 0x3880 reaches its own bit 15 exactly when it is
+// at least 0x4780, and the low half (at most 0xb87f) never carries into the
+// high one.
+__device__ __forceinline__ uint32_t bf16x2_past_f16(uint32_t w) {
+  return ((w & 0x7fff7fffu) + 0x38803880u) & 0x80008000u;
+}
 
 // Named barrier over `nthreads` threads (whole warps).  bar.sync is the
 // warp-aligned form: a warp must reach it with all lanes together, and a warp
@@ -334,6 +348,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(

@@ -15,12 +15,17 @@
 #include "fa_ptx.cuh"
 #include "fa_row.cuh"
 
-// Device error word: FA_DEV_ERR_* bits OR-ed in by every kernel of the library.
-__device__ unsigned int g_fa_device_error;
+// Device error words: one per live cache descriptor (the cache's slot), where
+// every kernel a call on that cache launches ORs its FA_DEV_ERR_* bits.
+// File-scope device storage: nothing is allocated for them.
+__device__ unsigned int g_fa_device_error[FA_MAX_CACHES];
 
 namespace fa {
 
-unsigned int* device_error_word(cudaError_t* err) {
+// Base of the error words on the current device.  In host code the array's
+// name is a host-side stand-in, so its device address is looked up once per
+// device, with that device current.
+static unsigned int* device_error_words(cudaError_t* err) {
   static std::mutex mu;
   static unsigned int* ptrs[128] = {};
   int dev = 0;
@@ -43,36 +48,81 @@ unsigned int* device_error_word(cudaError_t* err) {
   return ptrs[dev];
 }
 
-// One (token, KV head, K or V) row per warp; `warp` counts the launch's
-// warps for this layer.
+unsigned int* device_error_word(const fa_cache* c, cudaError_t* err) {
+  unsigned int* base = device_error_words(err);
+  return base ? base + c->err_slot : nullptr;
+}
+
+cudaError_t clear_device_error_word(const fa_cache* c) {
+  cudaError_t e;
+  unsigned int* w = device_error_word(c, &e);
+  if (!w) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+}
+
+// R consecutive (token, KV head, K or V) rows per warp, `warp` counting the
+// launch's warps for this layer.  The warp first loads the R slots, then all
+// R rows (R * D / 256 16-byte vectors per lane in flight), then stores them:
+// with one row per warp the store was bound by the latency of its two
+// dependent loads, not by bandwidth.
+template <int D>
+struct StoreShape {
+  static constexpr int R = D == 256 ? 4 : 2;   // rows per warp: 64 bytes per lane in flight
+};
+
 template <int D, int KV>
-__device__ __forceinline__ void store_row(const StoreArgs& a, int warp, int lane) {
+__device__ __forceinline__ void store_rows(const StoreArgs& a, int warp, int lane) {
+  constexpr int R = StoreShape<D>::R;
   const int rows = a.T * a.Hkv * 2;
-  if (warp >= rows) return;
-  const int which = warp & 1;            // 0: K, 1: V
-  const int th = warp >> 1;
-  const int t = th / a.Hkv, h = th % a.Hkv;
-  const int slot = __ldg(a.slots + t);
-  if (slot < 0) return;                  // padding token
-  const int page = slot / a.page_size, off = slot % a.page_size;
-  if (page >= a.num_pages) {
-    if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
-    return;
+  const int r0 = warp * R;
+  if (r0 >= rows) return;
+  size_t dst[R];
+  bool ok[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int row = r0 + i;
+    ok[i] = false;
+    dst[i] = 0;
+    if (row < rows) {
+      const int th = row >> 1;   // row = 2 * (t * Hkv + h) + (0: K, 1: V)
+      const int t = th / a.Hkv, h = th % a.Hkv;
+      const int slot = __ldg(a.slots + t);
+      if (slot >= 0) {           // a negative slot is a padding token
+        const int page = slot / a.page_size, off = slot % a.page_size;
+        if (page >= a.num_pages) {
+          if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
+        } else {
+          ok[i] = true;
+          dst[i] = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
+        }
+      }
+    }
   }
   griddep_wait();   // the rows (and the slab) may belong to the previous kernel
-  RowRegs<D> r;
-  row_load<D>(r, static_cast<const __nv_bfloat16*>(which ? a.v : a.k) + (static_cast<size_t>(t) * a.Hkv + h) * D, lane);
-  const size_t row = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
+  RowRegs<D> r[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int row = r0 + i;
+    if (ok[i])
+      row_load<D>(r[i], static_cast<const __nv_bfloat16*>((row & 1) ? a.v : a.k) + static_cast<size_t>(row >> 1) * D,
+                  lane);
+  }
   constexpr size_t elem = KV == FA_KV_BF16 ? 2 : 1;
-  row_store<D, KV>(r, static_cast<uint8_t*>(which ? a.v_slab : a.k_slab) + row * D * elem,
-                   KV == FA_KV_BF16 ? nullptr : (which ? a.v_scale : a.k_scale) + row, lane);
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int which = (r0 + i) & 1;
+    if (ok[i])
+      row_store<D, KV>(r[i], static_cast<uint8_t*>(which ? a.v_slab : a.k_slab) + dst[i] * D * elem,
+                       KV == FA_KV_BF16 ? nullptr : (which ? a.v_scale : a.k_scale) + dst[i], lane);
+  }
 }
 
 template <int D, int KV>
 __global__ void __launch_bounds__(256) store_kernel(StoreArgs a) {
   if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
-  store_row<D, KV>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
+  store_rows<D, KV>(a, (blockIdx.x * blockDim.x + threadIdx.x) >> 5, threadIdx.x & 31);
 }
 
 // Several layers' stores in one launch: blockIdx.y picks the layer.
@@ -86,8 +136,15 @@ __global__ void __launch_bounds__(256) store_layers_kernel(const __grid_constant
   if (!a.early_metadata) griddep_wait();
   griddep_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (a.D == 256) store_row<256, KV>(a, warp, lane);
-  else store_row<512, KV>(a, warp, lane);
+  if (a.D == 256) store_rows<256, KV>(a, warp, lane);
+  else store_rows<512, KV>(a, warp, lane);
+}
+
+// Warps a store of T tokens needs.
+static long store_warps(const StoreArgs& a) {
+  const long rows = static_cast<long>(a.T) * a.Hkv * 2;
+  const int R = a.D == 256 ? StoreShape<256>::R : StoreShape<512>::R;
+  return (rows + R - 1) / R;
 }
 
 cudaError_t launch_store_layers(const StoreArgs* a, int n, cudaStream_t s) {
@@ -96,7 +153,7 @@ cudaError_t launch_store_layers(const StoreArgs* a, int n, cudaStream_t s) {
   long warps = 0;
   for (int i = 0; i < n; ++i) {
     m.a[i] = a[i];
-    warps = std::max(warps, static_cast<long>(a[i].T) * a[i].Hkv * 2);
+    warps = std::max(warps, store_warps(a[i]));
   }
   const int block = 256;
   const long grid = (warps * 32 + block - 1) / block;
@@ -108,7 +165,7 @@ cudaError_t launch_store_layers(const StoreArgs* a, int n, cudaStream_t s) {
 }
 
 cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {
-  const long warps = static_cast<long>(a.T) * a.Hkv * 2;
+  const long warps = store_warps(a);
   const int block = 256;
   const long grid = (warps * 32 + block - 1) / block;
   if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
@@ -125,10 +182,11 @@ cudaError_t launch_store(const StoreArgs& a, cudaStream_t s) {
 
 }  // namespace fa
 
-extern "C" fa_status fa_get_device_error(int32_t* code, void* stream) {
+extern "C" fa_status fa_get_device_error(fa_cache* cache, int32_t* code, void* stream) {
+  if (!cache) return fa::fail(FA_ERR_INVALID_ARG, "cache is NULL");
   if (!code) return fa::fail(FA_ERR_INVALID_ARG, "code is NULL");
   cudaError_t ce;
-  unsigned int* p = fa::device_error_word(&ce);
+  unsigned int* p = fa::device_error_word(cache, &ce);
   if (!p) return fa::fail(FA_ERR_CUDA, "device error word: %s", cudaGetErrorString(ce));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned int v = 0;

@@ -34,8 +34,11 @@
  *   (thread-local).  Launch failures return FA_ERR_CUDA.  Faults that only the
  *   device can see (a page id outside [0, num_pages), a slot outside the pool,
  *   a sequence longer than the bound the caller promised, a bounded wait that
- *   ran out) never trap: the kernel skips the access, sets a bit in a device
- *   error word and finishes; fa_get_device_error() reads and clears it.
+ *   ran out) never trap: the kernel skips the access, sets a bit in the
+ *   cache's device error word and finishes; fa_get_device_error() reads and
+ *   clears it.  Each live cache has a word of its own (a slot of a fixed
+ *   device array of FA_MAX_CACHES words, one array per device), so calls on
+ *   one cache never see or clear another cache's errors.
  * - Types.  bf16 tensors are IEEE bfloat16 (2 bytes); int32 tables are
  *   little-endian int32_t; all tensors are dense row-major with the shapes
  *   given below.  Device pointers must be 16-byte aligned.
@@ -99,6 +102,15 @@ typedef enum { FA_FULL = 0, FA_SLIDING = 1 } fa_layer_kind;
 #define FA_DEV_ERR_BOUND 0x4u      /* a length exceeded the caller's max bound      */
 #define FA_DEV_ERR_TIMEOUT 0x8u    /* a bounded barrier wait ran out                */
 #define FA_DEV_ERR_WORKSPACE 0x10u /* decode workspace counters were not zero      */
+#define FA_DEV_ERR_RANGE 0x20u     /* a value out of the kernels' range: an f16
+                                      operand saturated (8-bit formats: a q, k or v
+                                      magnitude of 65520 or more), or an extend
+                                      score with |sm_scale * q.k| * log2(e) of
+                                      32767 or more                                 */
+
+/* Most fa_cache descriptors that may be live at once (each holds one device
+ * error word). */
+#define FA_MAX_CACHES 4096
 
 /* One attention layer.  kind: fa_layer_kind.  head_dim: 256 or 512 (other
  * widths return FA_ERR_UNSUPPORTED; the pages name exactly these two).
@@ -127,7 +139,8 @@ typedef struct fa_cache fa_cache;   /* opaque host-side descriptor */
  * head_dim / num_kv_heads differ (review thread of the same PR: such a
  * layout is refused, not served).  page_size must be a multiple of 16 and at
  * most 256.  On success *out receives a descriptor to free with
- * fa_cache_destroy.  Host only; no CUDA call. */
+ * fa_cache_destroy.  At most FA_MAX_CACHES descriptors may be live at once
+ * (FA_ERR_UNSUPPORTED beyond).  Host only; no CUDA call. */
 FA_API fa_status fa_cache_create(const fa_layer_desc* layers, int32_t n_layers, int32_t num_pages,
                           int32_t page_size, int32_t kv_dtype, fa_cache** out);
 
@@ -175,8 +188,10 @@ FA_API fa_status fa_cache_slab_bytes(const fa_cache* cache, int32_t layer, size_
  * layout above; k_scale, v_scale required in the 8-bit formats, ignored in
  * bf16).  Binding a shared layer returns FA_ERR_INVALID_ARG: it reads its
  * source's slab.  Rebinding replaces the previous pointers.  Encodes the TMA
- * descriptors the kernels use, so it needs a CUDA device (FA_ERR_CUDA when the
- * driver cannot be reached). */
+ * descriptors the kernels use and clears the cache's device error word on
+ * the current device (synchronously: do not call it during stream capture),
+ * so it needs a CUDA device (FA_ERR_CUDA when the driver cannot be
+ * reached). */
 FA_API fa_status fa_cache_bind_slab(fa_cache* cache, int32_t layer, void* k, void* v, float* k_scale,
                              float* v_scale);
 
@@ -226,7 +241,9 @@ FA_API size_t fa_decode_workspace_bytes(const fa_cache* cache, int32_t layer, in
  * FA_DEV_ERR_BOUND and are cut at the bound).
  * out: bf16 [B][Hq][D].  lse: optional float [B][Hq], natural-log
  * sum-exp of the scaled scores.  seq_lens[b] <= 0 gives out = 0 and
- * lse = -inf.  workspace: device scratch of at least
+ * lse = -inf.  Over 8-bit slabs q is converted to f16 for the tensor cores:
+ * an element of magnitude 65536 or more saturates to +-65504 and sets
+ * FA_DEV_ERR_RANGE.  workspace: device scratch of at least
  * fa_decode_workspace_bytes(cache, layer, B, max_seq_len) bytes (may be NULL
  * when that is 0), 256-byte aligned.  Zero it once before its first use: its
  * leading counters must start at zero, and every call that completes leaves
@@ -344,7 +361,17 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * P_b + j, j <= i (from k_ext / v_ext, bf16, never quantised), under the
  * layer's mask.  Over 8-bit slabs every tensor-core operand (q, the
  * dequantised and the chunk k, v, and the softmax weights) is f16, with fp32
- * accumulation; magnitudes past the f16 range (65504) saturate.
+ * accumulation.  Range: a q, k_ext or v_ext element of magnitude 65536 or
+ * more (bf16 has nothing between 65280 and 65536, f16 nothing past 65504),
+ * or a prefix row whose largest dequantised magnitude (127 or 448 times its
+ * scale) reaches 65520, saturates to +-65504 and sets FA_DEV_ERR_RANGE; the
+ * output is then not the exact attention.  At the small end, dequantised
+ * values below f16's smallest normal (6.1e-5) are kept as f16 subnormals in
+ * steps of 2^-24 (6e-8): rows whose largest magnitude is above about 1e-4
+ * keep the stated float tolerance; much smaller rows lose relative accuracy
+ * without an error bit.  Every slab format: a scaled score |sm_scale * q.k|
+ * of 32767 / log2(e) (about 22700) or more is out of range (FA_DEV_ERR_RANGE;
+ * the two softmax halves of a row agree on an integer base, kept in 16 bits).
  * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
  * (for a shared layer: the source layer's current k, v).  qo_indptr: int32
  * [B+1], non-decreasing, qo_indptr[0] = 0.  num_tokens: the rows of q, k_ext,
@@ -384,9 +411,10 @@ FA_API fa_status fa_paged_decode_multi_attn(fa_cache* cache, int32_t layer, cons
                                             int32_t max_q_len, int32_t max_seq_len, void* out, float* lse,
                                             void* stream);
 
-/* Synchronise `stream`, then read and clear the device error word of the
- * current device (FA_DEV_ERR_* bits; 0 = no error). */
-FA_API fa_status fa_get_device_error(int32_t* code, void* stream);
+/* Synchronise `stream`, then read and clear the device error word of
+ * `cache` on the current device (FA_DEV_ERR_* bits of every kernel launched
+ * by calls on this cache since the last read; 0 = no error). */
+FA_API fa_status fa_get_device_error(fa_cache* cache, int32_t* code, void* stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 FA_API const char* fa_last_error(void);

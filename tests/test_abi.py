@@ -245,3 +245,31 @@ def test_extend_argument_checks(fa):
                                     None) == fa.ERR_NOT_BOUND
     assert lib.fa_paged_extend_attn(c._h, 3, None, None, None, None, None, None, 4, 1, 8, 8, 16, None, None,
                                     None) == fa.ERR_INVALID_ARG                       # no layer 3
+
+
+def test_live_caches_hold_error_word_slots(fa):
+    """Each live cache holds one slot of the fixed device array of error
+    words: creation beyond FA_MAX_CACHES live descriptors is refused, and a
+    destroyed descriptor's slot serves the next one (host only, no GPU)."""
+    lib = fa.lib()
+    arr = (fa.LayerDesc * 1)(fa._desc(lay(FULL, 512, 8, 1)))
+    handles = []
+    try:
+        while len(handles) <= fa.MAX_CACHES:
+            h = ctypes.c_void_p()
+            st = lib.fa_cache_create(arr, 1, 8, 16, fa.KV_BF16, ctypes.byref(h))
+            if st != fa.OK:
+                assert st == fa.ERR_UNSUPPORTED and b"live" in lib.fa_last_error()
+                break
+            handles.append(h)
+        # other tests of this process may hold a few caches
+        assert fa.MAX_CACHES - 64 <= len(handles) < fa.MAX_CACHES + 1
+        lib.fa_cache_destroy(handles.pop())
+        h = ctypes.c_void_p()
+        assert lib.fa_cache_create(arr, 1, 8, 16, fa.KV_BF16, ctypes.byref(h)) == fa.OK
+        handles.append(h)
+    finally:
+        for h in handles:
+            lib.fa_cache_destroy(h)
+    code = ctypes.c_int32()
+    assert lib.fa_get_device_error(None, ctypes.byref(code), None) == fa.ERR_INVALID_ARG

@@ -170,9 +170,13 @@ def test_e2b_decode_full_size():
 
 
 def test_long_context_decode_full_size():
+    """Contexts of 32k-131k tokens: the longest sequence is always checked (the
+    split-K merges with the most partials), with both owning sliding layers,
+    the owning full layer and shared layers of both kinds."""
     w = W.long_decode()
     case = DecodeCase(w.layers, W.seq_lens(w), w.page_size, w.kv_dtype, w.seed, window_table=True, poison=True)
-    check_layers(case, _sample(case.B, 3, 3), layers=[0, 4, 7, 9])
+    seqs = sorted(set(_sample(case.B, 3, 3) + [int(np.argmax(case.lens))]))
+    check_layers(case, seqs, layers=[0, 4, 6, 7, 9, 11])
 
 
 @pytest.mark.parametrize("make", [W.int8_decode, W.fp8_decode], ids=["int8", "fp8"])

@@ -192,3 +192,20 @@ def test_chunked_prefill_workload():
             idx = torch.tensor(toks)
             assert_close(out[idx], ref[toks], what=f"chunk {ci} layer {li}")
         assert c.fa.device_error() == 0
+
+
+def test_large_scores_keep_parity_and_report_out_of_range():
+    """A chunk key of 65280 makes its scores reach thousands (log2 units): the
+    two softmax halves of a row still agree on an exact base and the result
+    matches the oracle.  A score past the 16-bit base range (a q element and
+    a key element of 60000) is reported as FA_DEV_ERR_RANGE."""
+    for layer in (lay(W.SLIDING, 256, 8, 2, 64), lay(W.FULL, 512, 8, 1)):
+        c = ExtendCase([layer], [40, 100], [37, 130], seed=11)
+        c.kx[0][5, 0, 3] = 65280.0
+        out = c.run(0)
+        assert_close(out, c.oracle(0), what="large key")
+        assert c.fa.device_error() == 0
+        c.q[0][20, 0, 3] = 60000.0
+        c.kx[0][5, 0, 3] = 60000.0
+        c.run(0)
+        assert c.fa.device_error() == c.fa.DEV_ERR_RANGE

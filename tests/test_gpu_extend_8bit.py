@@ -29,9 +29,12 @@ def lay(kind, D, hq, hkv, Wn=0, src=W.KV_OWN):
 class Case8:
     """Sequences with prefix_b stored tokens and chunk_b new ones.  With
     `store_chunk` the new tokens' rows are stored too (multi-token decode
-    reads every key from the slab)."""
+    reads every key from the slab).  `mag` scales every k, v row (prefix and
+    chunk) before it is rounded to bf16; `poke(kp, vp)` may edit the prefix
+    rows before they are stored."""
 
-    def __init__(self, layers, prefix, chunk, kv_dtype, seed, page_size=16, store_chunk=False):
+    def __init__(self, layers, prefix, chunk, kv_dtype, seed, page_size=16, store_chunk=False, mag=1.0,
+                 poke=None):
         import full_attention_gb300 as fa
         self.fa, self.layers, self.kv, self.ps = fa, layers, kv_dtype, page_size
         self.prefix = np.asarray(prefix, np.int32)
@@ -58,11 +61,16 @@ class Case8:
             v_s.fill_(0xFF if kv_dtype == W.KV_FP8 else -77)
             ks_s.fill_(float("nan"))
             vs_s.fill_(float("nan"))
-            self.kx[o] = W.randn_bf16((max(self.N, 1), H, D), seed * 100 + 21 + 3 * o, dev)
-            self.vx[o] = W.randn_bf16((max(self.N, 1), H, D), seed * 100 + 22 + 3 * o, dev)
+            def gen(shape, sd):
+                x = W.randn_bf16(shape, sd, dev)
+                return x if mag == 1.0 else (x.float() * mag).to(torch.bfloat16)
+            self.kx[o] = gen((max(self.N, 1), H, D), seed * 100 + 21 + 3 * o)
+            self.vx[o] = gen((max(self.N, 1), H, D), seed * 100 + 22 + 3 * o)
             npre = int(self.prefix.sum())
-            kp = W.randn_bf16((max(npre, 1), H, D), seed * 100 + 40 + 2 * o, dev)[:npre]
-            vp = W.randn_bf16((max(npre, 1), H, D), seed * 100 + 41 + 2 * o, dev)[:npre]
+            kp = gen((max(npre, 1), H, D), seed * 100 + 40 + 2 * o)[:npre]
+            vp = gen((max(npre, 1), H, D), seed * 100 + 41 + 2 * o)[:npre]
+            if poke is not None:
+                poke(kp, vp)
             slots = [W.slots_for_positions(self.bt_np[b], np.arange(0, int(self.prefix[b])), page_size)
                      for b in range(self.B)]
             slots = np.concatenate(slots).astype(np.int32)
@@ -105,11 +113,11 @@ class Case8:
                           self.prefix_dev, self.bt, int(self.chunk.max()), int(max(self.prefix.max(), 0)), out, lse)
         return out[: self.N], lse[: self.N]
 
-    def oracle_extend(self, i):
+    def oracle_extend(self, i, rows=None):
         o = self.src[i]
         return oracle.paged_extend(self.layers, i, {o: self.oslabs[o]}, bits(self.q[i][: self.N]),
                                    bits(self.kx[o][: self.N]), bits(self.vx[o][: self.N]), self.indptr, self.prefix,
-                                   self.bt_np, self.ps)
+                                   self.bt_np, self.ps, rows=rows)
 
     def decode_multi(self, i):
         out, lse = self._out(i)
@@ -200,3 +208,104 @@ def test_8bit_extend_edges(spec, kv_dtype):
     c = Case8([layer], prefix, chunk, kv_dtype, seed=34, page_size=ps)
     _check(c.extend(0), c.oracle_extend(0), "8-bit extend edge")
     assert c.fa.device_error() == 0
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+def test_8bit_chunked_prefill_workload(kv_dtype):
+    """The chunked-prefill workload (4 prompts of 4096 tokens in 512-token
+    chunks, sliding D 256 W 1024 with 16 q / 8 KV heads and full D 512 with
+    16 q / 2 KV heads) over 8-bit slabs, at full size: chunks 0, 3 and 7 of
+    both layers, on sampled rows that include the first and last rows and the
+    boundary between the first two sequences, every query head of each."""
+    w = W.chunked_prefill()
+    B, Cn = w.batch, w.chunk
+    rng = np.random.default_rng(5)
+    for ci in (0, 3, 7):
+        P = ci * Cn
+        c = Case8(w.layers, [P] * B, [Cn] * B, kv_dtype, seed=40 + ci)
+        for li in range(len(w.layers)):
+            out, lse = c.extend(li)
+            d = w.layers[li]
+            toks = sorted(set(rng.choice(c.N, size=16, replace=False).tolist() + [0, c.N - 1, Cn - 1, Cn]))
+            rows = [(t, j) for t in toks for j in range(d["num_q_heads"])]
+            ref_out, ref_lse = c.oracle_extend(li, rows=rows)
+            idx = torch.tensor(toks)
+            _check((out[idx], lse[idx]), (ref_out[toks], ref_lse[toks]), f"{IDS[FORMATS.index(kv_dtype)]} chunk {ci} layer {li}")
+        assert c.fa.device_error() == 0
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+@pytest.mark.parametrize("mag", [1e-3, 1e-4], ids=["1e-3", "1e-4"])
+def test_8bit_extend_small_magnitudes(mag, kv_dtype):
+    """Rows of small magnitude: dequantised values (and chunk values) fall
+    below f16's smallest normal number (6.1e-5) and are kept as f16
+    subnormals; rows down to about 1e-4 stay within the float tolerance."""
+    for layer in (lay(W.SLIDING, 256, 8, 2, 64), lay(W.FULL, 512, 8, 1)):
+        c = Case8([layer], [70, 150], [90, 33], kv_dtype, seed=35, mag=mag)
+        _check(c.extend(0), c.oracle_extend(0), f"small rows x{mag}")
+        assert c.fa.device_error() == 0
+
+
+BIG_IN, BIG_OUT = 65280.0, 65536.0   # the bf16 values on either side of f16's largest (65504)
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+def test_8bit_extend_f16_range_inside(kv_dtype):
+    """Values of 65280, just inside the f16 range, set no error bit.  With
+    them in a chunk key row and a stored prefix key row the result also
+    matches the oracle: those keys win or lose their softmax rows by
+    thousands, a well-conditioned case.  A q element that large is not
+    compared: its scores against the other (dequantised, f16-rounded) keys
+    are about 4000 times the key values, so a rounding of one part in 2^12
+    moves them by several units and the softmax weights with them, on any
+    f16 path.  q, V and the prefix V rows are checked for the error bit."""
+    def poke_k(kp, vp):
+        kp[3, 0, 5] = -BIG_IN
+    c = Case8([lay(W.FULL, 256, 4, 1)], [40, 20], [30, 10], kv_dtype, seed=36, poke=poke_k)
+    c.kx[0][2, 0, 0] = BIG_IN
+    _check(c.extend(0), c.oracle_extend(0), "key values at 65280")
+    assert c.fa.device_error() == 0
+
+    def poke_v(kp, vp):
+        vp[7, 0, 9] = BIG_IN
+    c = Case8([lay(W.FULL, 256, 4, 1)], [40, 20], [30, 10], kv_dtype, seed=36, poke=poke_v)
+    c.q[0][4, 1, 11] = BIG_IN
+    c.vx[0][5, 0, 7] = -BIG_IN
+    c.extend(0)
+    assert c.fa.device_error() == 0
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+@pytest.mark.parametrize("where", ["q", "k_ext", "v_ext", "prefix_k", "prefix_v"])
+def test_8bit_extend_f16_range_outside_sets_error_bit(where, kv_dtype):
+    """A value of 65536, just past the f16 range, in q, in a chunk row or in
+    a stored prefix row: the kernel saturates it and sets FA_DEV_ERR_RANGE."""
+    def poke(kp, vp):
+        if where == "prefix_k":
+            kp[3, 0, 5] = BIG_OUT
+        if where == "prefix_v":
+            vp[7, 0, 9] = -BIG_OUT
+    c = Case8([lay(W.FULL, 256, 4, 1)], [40, 20], [30, 10], kv_dtype, seed=37, poke=poke)
+    if where == "q":
+        c.q[0][4, 1, 11] = BIG_OUT
+    if where == "k_ext":
+        c.kx[0][2, 0, 0] = -BIG_OUT
+    if where == "v_ext":
+        c.vx[0][5, 0, 7] = BIG_OUT
+    c.extend(0)
+    assert c.fa.device_error() == c.fa.DEV_ERR_RANGE
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+def test_8bit_decode_f16_range(kv_dtype):
+    """8-bit decode converts q to f16: 65280 passes without an error bit,
+    65536 saturates and sets FA_DEV_ERR_RANGE."""
+    c = Case8([lay(W.FULL, 512, 8, 1)], [40, 90], [1, 1], kv_dtype, seed=38, store_chunk=True)
+    max_len = int(c.lens_dev.max())
+    ws = c.fa.workspace(c.cache.decode_workspace_bytes(0, c.B, max_len))
+    for val, want in ((BIG_IN, 0), (BIG_OUT, c.fa.DEV_ERR_RANGE)):
+        q = c.q[0][: c.N].clone()
+        q[1, 3, 100] = val
+        out = torch.empty_like(q)
+        c.cache.decode(0, q, c.bt, c.lens_dev, max_len, out, None, ws)
+        assert c.fa.device_error() == want
