@@ -871,9 +871,15 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
 // they work.  P (bf16) goes to shared memory as the A operand of the PV MMA
 // (two 64-key blocks in the 128-byte-swizzled K-major layout), written once
 // the previous PV has read it.
-// The K/V ring holds 16 KB chunks (128 keys x 64 columns); a tile's K passes
-// as KB chunks, its V slice as 4 chunks in 4 consecutive slots, so the ring
-// length (a multiple of 4) never splits the V group the N = 256 MMA spans.
+// The K/V ring holds 16 KB slots.  A tile's K passes as KB chunks of 128 keys
+// x 64 columns (page groups of 16 rows by TMA, 2 KB each: the 128-byte
+// swizzle span).  Its V slice passes as 4 slots in a row (the ring length is
+// a multiple of 4, so the group never wraps), laid out by page group: each
+// group's 16 keys x 256 columns come in one 8 KB TMA box of 4 column blocks,
+// so the PV MMA for keys 16ks .. 16ks + 15 reads group ks (column blocks 2 KB
+// apart: its LBO).  Copies made by cp.async (page groups the prefix end or
+// the window start cut, or without a page) are flagged per slot, and the MMA
+// warp fences only those slots for its async-proxy reads.
 // Roles as above: warps 0-3 fill ring slot e (warp e % 4), TMA for page
 // groups 0-3 of a prefix chunk and cp.async for groups 4-7; warp 4 issues the
 // MMAs; warps 5-12 run the softmax, two per tensor-memory lane quarter, each
@@ -901,7 +907,7 @@ struct E128Cfg {
   static constexpr int OFF_BAR = OFF_RING + NSLOT * CHUNK;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
-  static constexpr int TMA_GROUPS = NGRP / 2;   // page groups by TMA, the rest by cp.async
+  static constexpr int TMA_GROUPS = NGRP;       // every whole page group goes by TMA
   static constexpr int NPW = 4;                 // producer warps
   static constexpr int W_MMA = NPW;
   static constexpr int NSMX = 8;                // softmax warps
@@ -914,15 +920,15 @@ struct E128Cfg {
   static_assert(NSLOT % 4 == 0 && NSLOT >= 8, "ring of whole V groups");
   static_assert(NPW <= NSLOT, "producer stride within one ring lap");
   static_assert(SMEM_ALLOC + 1024 <= 232448, "shared memory budget");
-  static_assert((1 + 2 * NSLOT + 6) * 8 + 8 <= BAR_BYTES, "barrier space");
+  static_assert((1 + 2 * NSLOT + 6) * 8 + 8 + NSLOT * 4 <= BAR_BYTES, "barrier space");
   static_assert(OFF_P % 1024 == 0 && OFF_RING % 1024 == 0 && CHUNK % 1024 == 0, "swizzle atoms");
 };
 
 template <int D>
 __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
     extend128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kx,
-                     const __grid_constant__ CUtensorMap tm_vx, const ExtK p) {
+                     const __grid_constant__ CUtensorMap tm_vg, const __grid_constant__ CUtensorMap tm_kx,
+                     const __grid_constant__ CUtensorMap tm_vxg, const ExtK p) {
   using C = E128Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -939,6 +945,9 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
   uint64_t* qt_full = o_bar + 1;        // the softmax warps have put Q into tensor memory
   uint64_t& done_bar = qt_full[1];      // every MMA has completed (before tensor memory is freed)
   uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(qt_full + 2);
+  // per ring slot: 1 when its last fill used cp.async (generic-proxy writes the
+  // MMA warp must fence for its async-proxy reads), 0 when TMA alone filled it
+  volatile uint32_t* slot_cp = reinterpret_cast<volatile uint32_t*>(qt_full + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!p.early_metadata) griddep_wait();
@@ -989,9 +998,9 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
     }
     if (lane == 0) {
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_vg);
       prefetch_tmap(&tm_kx);
-      prefetch_tmap(&tm_vx);
+      prefetch_tmap(&tm_vxg);
     }
     const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
     struct PageRef {
@@ -1013,6 +1022,7 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
     };
     struct TileSrc {
       int row0[C::NGRP];   // slab row of each 16-row group (prefix tiles), -1: no page
+      int my_row0;         // lane g < NGRP: row0[g]
       int lim;             // rows [0, lim) of the tile hold keys
       int wlim;            // rows below wlim precede every visible key of the CTA: read as zero
       int bgroup;          // the group holding the prefix end inside it, -1: none
@@ -1037,59 +1047,128 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
       }
 #pragma unroll
       for (int g = 0; g < C::NGRP; ++g) ts.row0[g] = __shfl_sync(0xffffffffu, r0, g);
+      ts.my_row0 = r0;
       return ts;
     };
-    auto by_tma = [&](const TileSrc& ts, int g) {
-      return g < C::TMA_GROUPS && g != ts.bgroup && ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
+    // group g of a prefix tile goes by TMA: a whole page group of readable keys
+    auto tma_group = [&](const TileSrc& ts, int g, int row0) {
+      return g < C::TMA_GROUPS && g != ts.bgroup && row0 >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
     };
+    auto by_tma = [&](const TileSrc& ts, int g) { return tma_group(ts, g, ts.row0[g]); };
     int e = 0;
     bool ok = true;
-    // one slot: column block blk (64 columns) of the tile's K or V rows
-    auto emit = [&](const TileSrc& ts, int blk, bool is_v) {
+    // lane 0 records whether this fill of slot sl uses cp.async before its
+    // first arrival on full[sl]: the barrier publishes it to the MMA warp
+    auto mark = [&](int sl, bool any_cp) {
+      if (lane == 0) slot_cp[sl] = any_cp ? 1u : 0u;
+    };
+    // wait until ring slot e is free; returns its slot index, -1 on a timeout
+    auto claim = [&]() -> int {
+      const int sl = e % C::NSLOT;
+      bool w = true;
+      if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+      ok = __shfl_sync(0xffffffffu, w, 0) && ok;
+      return ok ? sl : -1;
+    };
+    // K chunk: column block blk (64 columns) of the tile's 128 keys
+    auto emit_k = [&](const TileSrc& ts, int blk) {
       if (e % C::NPW == pw) {
-        const int sl = e % C::NSLOT;
-        bool w = true;
-        if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
-        ok = __shfl_sync(0xffffffffu, w, 0) && ok;
-        if (ok) {
+        const int sl = claim();
+        if (sl >= 0) {
           uint8_t* dst = ring + sl * C::CHUNK;
           if (ts.prefix) {
+            // lane g issues group g's box: the page groups' copies start
+            // together instead of one after another from a single thread
             if (lane == 0) {
               int tx = 0;
 #pragma unroll
               for (int g = 0; g < C::NGRP; ++g)
                 if (by_tma(ts, g)) tx += 2048;
+              slot_cp[sl] = tx == C::NGRP * 2048 ? 0u : 1u;
               mbar_arrive_expect_tx(&full[sl], tx);
-#pragma unroll
-              for (int g = 0; g < C::NGRP; ++g)
-                if (by_tma(ts, g))
-                  tma_load_3d(dst + g * 2048, is_v ? &tm_v : &tm_k, &full[sl], 0, blk, ts.row0[g], pol);
             }
-            const uint8_t* base = is_v ? p.v_slab : p.k_slab;
+            __syncwarp();
+            if (lane < C::NGRP && tma_group(ts, lane, ts.my_row0))
+              tma_load_3d(dst + lane * 2048, &tm_k, &full[sl], 0, blk, ts.my_row0, pol);
             bool any_cp = false;
 #pragma unroll
             for (int g = 0; g < C::NGRP; ++g) {
               if (by_tma(ts, g)) continue;
               any_cp = true;
-              // 16 rows x 8 units: lane copies rows lane / 8 + 4 i, unit lane % 8
+              // 16 rows x 8 units: lane copies rows lane / 8 + 4 i, unit lane % 8;
+              // rows holding no visible key read as zero (stale rows may be NaN)
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
                 const bool v = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
                 const uint8_t* src =
-                    base + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + blk * 64) * 2 + (lane & 7) * 16 : 0);
+                    p.k_slab + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + blk * 64) * 2 + (lane & 7) * 16 : 0);
                 cp_async16_zfill(dst + sw128(r, lane & 7), src, v, pol);
               }
             }
             if (any_cp) cp_async_mbar_arrive(&full[sl]);
             else if (lane == 0) mbar_arrive_n(&full[sl], 32);
           } else {
+            mark(sl, false);
+            if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::CHUNK);
+            __syncwarp();
+            if (lane < 2)   // two 64-row boxes, one per lane
+              tma_load_4d(dst + lane * (C::CHUNK / 2), &tm_kx, &full[sl], 0, blk, x.h, ts.tok0 + 64 * lane, pol);
+            if (lane == 0) mbar_arrive_n(&full[sl], 32);
+          }
+        }
+      }
+      ++e;
+    };
+    // V slot v of a tile: page groups 2v, 2v + 1, each 16 keys x the CTA's
+    // 256 columns ([4 column blocks][16 rows][128 B], 8 KB)
+    auto emit_v = [&](const TileSrc& ts, int v) {
+      if (e % C::NPW == pw) {
+        const int sl = claim();
+        if (sl >= 0) {
+          uint8_t* dst = ring + sl * C::CHUNK;
+          const int blk0 = x.ds * C::NVB;
+          if (ts.prefix) {
+            const int g_l = 2 * v + (lane & 1);   // lanes 0, 1: groups 2v, 2v + 1
+            const int r_l = __shfl_sync(0xffffffffu, ts.my_row0, g_l);
             if (lane == 0) {
-              mbar_arrive_expect_tx(&full[sl], C::CHUNK);
-              tma_load_4d(dst, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, ts.tok0, pol);
-              tma_load_4d(dst + C::CHUNK / 2, is_v ? &tm_vx : &tm_kx, &full[sl], 0, blk, x.h, ts.tok0 + 64, pol);
-              mbar_arrive_n(&full[sl], 32);
+              int tx = 0;
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if (by_tma(ts, 2 * v + h)) tx += 8192;
+              slot_cp[sl] = tx == 2 * 8192 ? 0u : 1u;
+              mbar_arrive_expect_tx(&full[sl], tx);
             }
+            __syncwarp();
+            if (lane < 2 && tma_group(ts, g_l, r_l))
+              tma_load_3d(dst + lane * 8192, &tm_vg, &full[sl], 0, r_l, blk0, pol);
+            bool any_cp = false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int g = 2 * v + h;
+              if (by_tma(ts, g)) continue;
+              any_cp = true;
+              const int row0 = __shfl_sync(0xffffffffu, ts.my_row0, g);
+              // 4 blocks x 16 rows x 8 units: lane copies units lane + 32 i
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int idx = lane + 32 * i, b = idx >> 7, rr = (idx >> 3) & 15, uu = idx & 7;
+                const int r = 16 * g + rr;
+                const bool ok_row = row0 >= 0 && r < ts.lim && r >= ts.wlim;
+                const uint8_t* src =
+                    p.v_slab + (ok_row ? (static_cast<size_t>(row0 + rr) * D + (blk0 + b) * 64) * 2 + uu * 16 : 0);
+                cp_async16_zfill(dst + h * 8192 + b * 2048 + sw128(rr, uu), src, ok_row, pol);
+              }
+            }
+            if (any_cp) cp_async_mbar_arrive(&full[sl]);
+            else if (lane == 0) mbar_arrive_n(&full[sl], 32);
+          } else {
+            mark(sl, false);
+            if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::CHUNK);
+            __syncwarp();
+            if (lane < 2)   // tokens of groups 2v, 2v + 1
+              tma_load_4d(dst + lane * 8192, &tm_vxg, &full[sl], 0, ts.tok0 + 16 * (2 * v + lane), x.h, blk0, pol);
+            if (lane == 0) mbar_arrive_n(&full[sl], 32);
           }
         }
       }
@@ -1102,10 +1181,10 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
         const PageRef pid = pid_next;
         pid_next = load_pid(t + 1);   // a tile ahead
         src_cur = tile_src(t, pid);
-        for (int kb = 0; ok && kb < C::KB; ++kb) emit(src_cur, kb, false);
+        for (int kb = 0; ok && kb < C::KB; ++kb) emit_k(src_cur, kb);
       }
       if (t >= 1)
-        for (int i = 0; ok && i < C::NVB; ++i) emit(src_prev, x.ds * C::NVB + i, true);
+        for (int v = 0; ok && v < C::NVB; ++v) emit_v(src_prev, v);
       src_prev = src_cur;
     }
     if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
@@ -1128,9 +1207,13 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
     const uint64_t pd0 = umma_desc_sw128(smem_u32(ps), 16, 1024);   // P's two key blocks
     const uint32_t s_tmem = tmem + C::S_COL0;
     int e = 0;
-    auto wait_slot = [&](int ee) -> uint32_t {   // wait for ring position ee, return its address
+    // wait for ring position ee, return its address; a slot that cp.async
+    // filled (partly) is fenced: those generic-proxy writes, seen through the
+    // barrier, are ordered before the MMAs' async-proxy reads
+    auto wait_slot = [&](int ee) -> uint32_t {
       const int sl = ee % C::NSLOT;
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[sl], (ee / C::NSLOT) & 1));
+      if (slot_cp[sl]) fence_proxy_async_smem();
       return smem_u32(ring + sl * C::CHUNK);
     };
     for (int t = 0; ok && t <= nt; ++t) {
@@ -1141,7 +1224,6 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
         for (int kb = 0; ok && kb < C::KB; ++kb) {
           const uint32_t kaddr = wait_slot(e);
           if (!ok) break;
-          fence_proxy_async_smem();   // the cp.async writes, seen through the barrier, for the MMA's reads
           tc_fence_after();
           // one descriptor per chunk; a K16 step advances 32 bytes along the
           // swizzled row (start-address field +2, no carry below 256 KB)
@@ -1176,14 +1258,15 @@ __global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
           if (v == 0) vaddr = a;
         }
         if (!ok) break;
-        fence_proxy_async_smem();
         tc_fence_after();
-        const uint64_t vd0 = umma_desc_sw128(vaddr, C::CHUNK, 1024);   // LBO: chunk stride along N
+        // V page group ks (8 KB apart) holds keys 16 ks .. 16 ks + 15; its 4
+        // column blocks lie 2 KB apart (LBO), its two 8-key halves 1 KB (SBO)
+        const uint64_t vd0 = umma_desc_sw128(vaddr, 2048, 1024);
         if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < C::NK / 16; ++ks)
             umma_ss(tmem, pd0 + static_cast<uint64_t>((ks >> 2) * (C::M * 128) / 16 + 2 * (ks & 3)),
-                    vd0 + static_cast<uint64_t>(ks * 2048 / 16), idO, (i > 0 || ks > 0) ? 1u : 0u);
+                    vd0 + static_cast<uint64_t>(ks * 8192 / 16), idO, (i > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
           for (int v = 0; v < C::NVB; ++v) umma_commit(&empty[(e + v) % C::NSLOT]);
           umma_commit(o_bar);   // PV_i completes phase i of o_bar
@@ -1421,19 +1504,20 @@ static cudaError_t launch_extend128_t(const ExtendArgs& a, const ExtK& k, cudaSt
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend128_kernel<D>), C::SMEM_ALLOC, &done);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
-  return launch_pdl(extend128_kernel<D>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
-                    a.tm_vx, k);
+  return launch_pdl(extend128_kernel<D>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_vg, a.tm_kx,
+                    a.tm_vxg, k);
 }
 
-// bf16 slabs take the 128-key kernel unless FA_EXTEND_TILE=64 selects the
-// 64-key one (both compute the same attention).
-static bool extend_tile64() {
+// bf16 slabs: head_dim 512 takes the 128-key kernel and head_dim 256 the
+// 64-key one, the faster of the two at each width (both compute the same
+// attention).  FA_EXTEND_TILE=64 or =128 selects one kernel for both widths.
+static int extend_tile(int D) {
   static int v = -1;
   if (v < 0) {
     const char* e = getenv("FA_EXTEND_TILE");
-    v = (e && e[0] == '6' && e[1] == '4') ? 1 : 0;
+    v = (e && e[0] == '6' && e[1] == '4') ? 64 : (e && e[0] == '1' && e[1] == '2' && e[2] == '8') ? 128 : 0;
   }
-  return v == 1;
+  return v ? v : (D == 512 ? 128 : 64);
 }
 
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
@@ -1474,7 +1558,7 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
     return a.D == 256 ? launch_extend_t<256, FA_KV_INT8>(a, k, s) : launch_extend_t<512, FA_KV_INT8>(a, k, s);
   if (a.kv_dtype == FA_KV_FP8)
     return a.D == 256 ? launch_extend_t<256, FA_KV_FP8>(a, k, s) : launch_extend_t<512, FA_KV_FP8>(a, k, s);
-  if (extend_tile64())
+  if (extend_tile(a.D) == 64)
     return a.D == 256 ? launch_extend_t<256, FA_KV_BF16>(a, k, s) : launch_extend_t<512, FA_KV_BF16>(a, k, s);
   return a.D == 256 ? launch_extend128_t<256>(a, k, s) : launch_extend128_t<512>(a, k, s);
 }
