@@ -151,15 +151,14 @@ static fa_status encode_slab_map(CUtensorMap* tm, void* base, int D, int kv_dtyp
 // block (stride 128 B).  A box (block, 16, D / block) is one 16-row tile that
 // lands as D / block consecutive 2 KB pieces of 16 rows x 128 B, each
 // 128-byte swizzled: the layout of the (block, 1, 16) boxes, in one copy.
-static fa_status encode_tile_map(CUtensorMap* tm, void* base, int D, int kv_dtype, uint64_t rows, int box_blocks = 0) {
+static fa_status encode_tile_map(CUtensorMap* tm, void* base, int D, int kv_dtype, uint64_t rows) {
   auto enc = get_encoder();
   if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const uint64_t eb = elem_bytes(kv_dtype);
   const uint64_t blk = 128 / eb;
   cuuint64_t dims[3] = {blk, rows, static_cast<cuuint64_t>(D / blk)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * eb), 128};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(kTile),
-                       static_cast<cuuint32_t>(box_blocks > 0 ? box_blocks : D / blk)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(kTile), static_cast<cuuint32_t>(D / blk)};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(tm, quantised(kv_dtype) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -198,23 +197,6 @@ static fa_status encode_ext_map(CUtensorMap* tm, const void* x, int N, int Hkv, 
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (k/v chunk) failed (CUresult %d)", (int)r);
-  return FA_OK;
-}
-
-// v_ext [N][Hkv][D] as 4-D (64 elements, token, KV head, 64-column block): a
-// box (64, 16, 1, 4) lands as 4 blocks x 16 token rows x 128 B, the layout of
-// the slab's page-group boxes (tm_vg).
-static fa_status encode_ext_group_map(CUtensorMap* tm, const void* x, int N, int Hkv, int D) {
-  auto enc = get_encoder();
-  if (!enc) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(D / 64)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(Hkv) * D * 2, static_cast<cuuint64_t>(D) * 2, 128};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTile), 1, 4};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled (v chunk groups) failed (CUresult %d)", (int)r);
   return FA_OK;
 }
 
@@ -424,8 +406,6 @@ fa_status fa_cache_bind_slab(fa_cache* c, int32_t layer, void* k, void* v, float
   if (st) return st;
   if ((st = encode_tile_map(&s.tm_kt, k, L.d.head_dim, c->kv_dtype, rows))) return st;
   if ((st = encode_tile_map(&s.tm_vt, v, L.d.head_dim, c->kv_dtype, rows))) return st;
-  if (quantised(c->kv_dtype)) s.tm_vg = s.tm_vt;   // extend over 8-bit slabs dequantises instead
-  else if ((st = encode_tile_map(&s.tm_vg, v, L.d.head_dim, c->kv_dtype, rows, 4))) return st;
   if (quantised(c->kv_dtype)) {
     if ((st = encode_scale_map(&s.tm_ks, k_scale, rows))) return st;
     if ((st = encode_scale_map(&s.tm_vs, v_scale, rows))) return st;
@@ -749,7 +729,6 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.tm_v = &s->tm_v;
   a.tm_ks = &s->tm_ks;
   a.tm_vs = &s->tm_vs;
-  a.tm_vg = &s->tm_vg;
   a.out = out;
   a.lse = lse;
   a.B = B;
@@ -771,7 +750,6 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   if ((st = encode_q_map(&a.tm_q, q, num_tokens, L.d.num_q_heads, L.d.head_dim, g))) return st;
   if ((st = encode_ext_map(&a.tm_kx, k_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
   if ((st = encode_ext_map(&a.tm_vx, v_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
-  if ((st = encode_ext_group_map(&a.tm_vxg, v_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
   ce = launch_extend(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "extend launch: %s", cudaGetErrorString(ce));
   return ok();
@@ -813,7 +791,6 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   a.tm_v = &s->tm_v;
   a.tm_ks = &s->tm_ks;
   a.tm_vs = &s->tm_vs;
-  a.tm_vg = &s->tm_vg;
   a.out = out;
   a.lse = lse;
   a.B = B;
@@ -835,7 +812,6 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   if ((st = encode_q_map(&a.tm_q, q, num_tokens, L.d.num_q_heads, L.d.head_dim, g))) return st;
   a.tm_kx = s->tm_k;   // no chunk rows in this mode: the chunk maps are never used
   a.tm_vx = s->tm_v;
-  a.tm_vxg = s->tm_vg;
   ce = launch_extend(a, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(ce));
   return ok();

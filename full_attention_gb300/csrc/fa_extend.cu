@@ -40,7 +40,6 @@
 // FA_DEV_ERR_RANGE.
 // Every wait is bounded; tensor memory is always freed.
 #include <cfloat>
-#include <cstdlib>
 
 #include <cuda_fp8.h>
 
@@ -127,7 +126,7 @@ struct ExtK {
 // different lines and the L2 slices share the load.  The softmax does not
 // depend on the order of the tiles.
 struct ExtPlan {
-  int nk;                  // keys per tile (64 or 128)
+  int nk;                  // keys per tile
   int b, h, ds, t0, n, P, qo0;
   int Pk;                  // keys [0, Pk) come from the slab (P, or all keys when keys_in_pages)
   int kmin, kmax;          // visible key positions of the CTA's rows
@@ -857,635 +856,6 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// bf16 slabs: 128-key tiles.
-//
-// An M = 128 tcgen05.mma costs about the same at N = 64 as at N = 128 (the
-// instruction rate, not the tensor pipe, bounds N = 64), so S = Q K^T over
-// 128 keys per tile takes half the MMAs of the 64-key kernel above, and PV
-// runs as one N = 256 MMA per 16 keys over the CTA's whole output slice.
-// Tensor memory (512 columns): O [0, 256), S [256, 384) (fp32, 128 keys),
-// and Q's first 256 columns as bf16 pairs [384, 512); Q's other 256 columns
-// (head_dim 512) stay in shared memory.  S has one buffer, released as soon
-// as the softmax warps hold it in registers, so S of the next tile runs while
-// they work.  P (bf16) goes to shared memory as the A operand of the PV MMA
-// (two 64-key blocks in the 128-byte-swizzled K-major layout), written once
-// the previous PV has read it.
-// The K/V ring holds 16 KB slots.  A tile's K passes as KB chunks of 128 keys
-// x 64 columns (page groups of 16 rows by TMA, 2 KB each: the 128-byte
-// swizzle span).  Its V slice passes as 4 slots in a row (the ring length is
-// a multiple of 4, so the group never wraps), laid out by page group: each
-// group's 16 keys x 256 columns come in one 8 KB TMA box of 4 column blocks,
-// so the PV MMA for keys 16ks .. 16ks + 15 reads group ks (column blocks 2 KB
-// apart: its LBO).  Copies made by cp.async (page groups the prefix end or
-// the window start cut, or without a page) are flagged per slot, and the MMA
-// warp fences only those slots for its async-proxy reads.
-// Roles as above: warps 0-3 fill ring slot e (warp e % 4), TMA for page
-// groups 0-3 of a prefix chunk and cp.async for groups 4-7; warp 4 issues the
-// MMAs; warps 5-12 run the softmax, two per tensor-memory lane quarter, each
-// thread one query row and 64 of a tile's 128 columns.
-template <int D>
-struct E128Cfg {
-  static constexpr int M = 128;                  // query rows per CTA
-  static constexpr int NK = 128;                 // keys per tile
-  static constexpr int NGRP = NK / 16;           // 16-row page groups per tile
-  static constexpr int DS = 256;                 // output columns per CTA
-  static constexpr int NVB = DS / 64;            // V chunks per tile
-  static constexpr int KB = D / 64;              // K chunks per tile (64 columns each)
-  static constexpr int NQT = 4;                  // Q blocks in tensor memory
-  static constexpr int NQS = KB - NQT;           // Q blocks in shared memory
-  static constexpr int CHUNK = NK * 128;         // 128 keys x 64 columns bf16
-  static constexpr int Q_BYTES = NQS * M * 128;  // [NQS][128 rows][128 B]
-  static constexpr int P_BYTES = 2 * M * 128;    // [2 key blocks][128 rows][128 B]
-  static constexpr int BAR_BYTES = 1024;
-  // dynamic shared memory: the opt-in maximum less the static array below
-  // (1 KB) and the 1 KB alignment slack
-  static constexpr int AVAIL = 232448 - 1024 - 1024;
-  static constexpr int NSLOT = (AVAIL - Q_BYTES - P_BYTES - BAR_BYTES) / CHUNK / 4 * 4;
-  static constexpr int OFF_P = Q_BYTES;
-  static constexpr int OFF_RING = OFF_P + P_BYTES;
-  static constexpr int OFF_BAR = OFF_RING + NSLOT * CHUNK;
-  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
-  static constexpr int SMEM_ALLOC = SMEM + 1024;
-  static constexpr int TMA_GROUPS = NGRP;       // every whole page group goes by TMA
-  static constexpr int NPW = 4;                 // producer warps
-  static constexpr int W_MMA = NPW;
-  static constexpr int NSMX = 8;                // softmax warps
-  static constexpr int NTHR = (NPW + 1 + NSMX) * 32;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL0 = DS;
-  static constexpr uint32_t Q_COL0 = DS + NK;
-  static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
-  static_assert(KB % 4 == 0 && NVB == 4, "a tile's K and V chunks come in groups of 4");
-  static_assert(NSLOT % 4 == 0 && NSLOT >= 8, "ring of whole V groups");
-  static_assert(NPW <= NSLOT, "producer stride within one ring lap");
-  static_assert(SMEM_ALLOC + 1024 <= 232448, "shared memory budget");
-  static_assert((1 + 2 * NSLOT + 6) * 8 + 8 + NSLOT * 4 <= BAR_BYTES, "barrier space");
-  static_assert(OFF_P % 1024 == 0 && OFF_RING % 1024 == 0 && CHUNK % 1024 == 0, "swizzle atoms");
-};
-
-template <int D>
-__global__ void __launch_bounds__(E128Cfg<D>::NTHR, 1)
-    extend128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_vg, const __grid_constant__ CUtensorMap tm_kx,
-                     const __grid_constant__ CUtensorMap tm_vxg, const ExtK p) {
-  using C = E128Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qs = smem;
-  uint8_t* ps = smem + C::OFF_P;
-  uint8_t* ring = smem + C::OFF_RING;
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* full = q_full + 1;          // [NSLOT]
-  uint64_t* empty = full + C::NSLOT;    // [NSLOT]
-  uint64_t* s_full = empty + C::NSLOT;  // S_t is in tensor memory
-  uint64_t* s_free = s_full + 1;        // every softmax warp holds S_t in registers
-  uint64_t* p_full = s_free + 1;        // P_t is in shared memory
-  uint64_t* o_bar = p_full + 1;         // PV_t has completed
-  uint64_t* qt_full = o_bar + 1;        // the softmax warps have put Q into tensor memory
-  uint64_t& done_bar = qt_full[1];      // every MMA has completed (before tensor memory is freed)
-  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(qt_full + 2);
-  // per ring slot: 1 when its last fill used cp.async (generic-proxy writes the
-  // MMA warp must fence for its async-proxy reads), 0 when TMA alone filled it
-  volatile uint32_t* slot_cp = reinterpret_cast<volatile uint32_t*>(qt_full + 3);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (!p.early_metadata) griddep_wait();
-  griddep_launch_dependents();
-  ExtPlan x;
-  if (!ext_plan<C::NK>(p, x)) return;
-  const int nt = x.tiles();
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(&full[i], 33);   // the filling warp: lane 0's expect_tx + 32 lane arrivals
-      mbar_init(&empty[i], 1);
-    }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, C::NSMX);
-    mbar_init(p_full, C::NSMX);
-    mbar_init(o_bar, 1);
-    mbar_init(qt_full, C::NSMX);
-    mbar_init(&done_bar, 1);
-    fence_mbar_init();
-  }
-  if (warp == C::W_MMA) tmem_alloc(&tmem_slot, C::TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_slot;
-  griddep_wait();   // from here on q, k, v, the slab and the outputs are touched
-
-  if (warp < C::NPW) {
-    // ----------------------------------------------------------- producers
-    // Emission order = the MMA issuer's consumption order: K_0, then for each
-    // t >= 1: K_t (if any) and V_{t-1}; slot e by warp e % NPW.  A prefix
-    // chunk is 8 page groups of 16 rows: groups 0-3 by TMA (one 2 KB box per
-    // group), groups 4-7 by the warp's cp.async copies; a group without a
-    // page, past the prefix end, before the window start or holding the
-    // prefix end goes by cp.async with zero fill (its stale rows, NaN
-    // included, must not reach the MMAs).  A chunk of k_ext / v_ext rows is
-    // two 64-row boxes.  full[] counts 33 arrivals: lane 0's expect_tx, then
-    // 32 lane arrivals (when their cp.async copies land, or at once).
-    const int pw = warp;
-    const uint64_t pol = l2_policy_evict_last();   // K/V rows are shared by the CTAs of a (sequence, head)
-    if (threadIdx.x == 0) {
-      prefetch_tmap(&tm_q);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int kb = C::NQT; kb < C::KB; ++kb)
-        tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
-    }
-    if (lane == 0) {
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_vg);
-      prefetch_tmap(&tm_kx);
-      prefetch_tmap(&tm_vxg);
-    }
-    const int32_t* bt = p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq;
-    struct PageRef {
-      int pid, off;
-    };
-    // page of row group `lane` (lanes 0-7) of tile j and the group's offset
-    // in it, looked up a tile ahead; the id is checked where it is used
-    auto load_pid = [&](int j) -> PageRef {
-      PageRef r{-1, 0};
-      if (j < nt && x.prefix(j) && lane < C::NGRP) {
-        const int pos = x.start(j) + 16 * lane;   // a 16-row group lies in one page
-        if (pos < x.Pk) {
-          const int q = pos / p.page_size;
-          r.off = pos - q * p.page_size;
-          r.pid = ld_nc_early(bt + q);
-        }
-      }
-      return r;
-    };
-    struct TileSrc {
-      int row0[C::NGRP];   // slab row of each 16-row group (prefix tiles), -1: no page
-      int my_row0;         // lane g < NGRP: row0[g]
-      int lim;             // rows [0, lim) of the tile hold keys
-      int wlim;            // rows below wlim precede every visible key of the CTA: read as zero
-      int bgroup;          // the group holding the prefix end inside it, -1: none
-      bool prefix;
-      int tok0;            // chunk tiles: first token row in k_ext / v_ext
-    };
-    auto tile_src = [&](int j, PageRef pr) {
-      TileSrc ts;
-      const int st0 = x.start(j);
-      ts.prefix = x.prefix(j);
-      ts.lim = ts.prefix ? x.Pk - st0 : x.n - (st0 - x.P);
-      ts.bgroup = (ts.prefix && ts.lim < C::NK && (ts.lim & 15) != 0) ? (ts.lim >> 4) : -1;
-      ts.tok0 = x.qo0 + st0 - x.P;
-      ts.wlim = ts.prefix ? max(0, x.kmin - st0) : 0;
-      int r0 = -1;
-      if (lane < C::NGRP && ts.prefix && 16 * lane < ts.lim) {
-        if (pr.pid < 0 || pr.pid >= p.num_pages) {
-          if (pw == 0) atomicOr(p.err, FA_DEV_ERR_PAGE);
-        } else {
-          r0 = (pr.pid * p.Hkv + x.h) * p.page_size + pr.off;
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < C::NGRP; ++g) ts.row0[g] = __shfl_sync(0xffffffffu, r0, g);
-      ts.my_row0 = r0;
-      return ts;
-    };
-    // group g of a prefix tile goes by TMA: a whole page group of readable keys
-    auto tma_group = [&](const TileSrc& ts, int g, int row0) {
-      return g < C::TMA_GROUPS && g != ts.bgroup && row0 >= 0 && 16 * g < ts.lim && 16 * g >= ts.wlim;
-    };
-    auto by_tma = [&](const TileSrc& ts, int g) { return tma_group(ts, g, ts.row0[g]); };
-    int e = 0;
-    bool ok = true;
-    // lane 0 records whether this fill of slot sl uses cp.async before its
-    // first arrival on full[sl]: the barrier publishes it to the MMA warp
-    auto mark = [&](int sl, bool any_cp) {
-      if (lane == 0) slot_cp[sl] = any_cp ? 1u : 0u;
-    };
-    // wait until ring slot e is free; returns its slot index, -1 on a timeout
-    auto claim = [&]() -> int {
-      const int sl = e % C::NSLOT;
-      bool w = true;
-      if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
-      ok = __shfl_sync(0xffffffffu, w, 0) && ok;
-      return ok ? sl : -1;
-    };
-    // K chunk: column block blk (64 columns) of the tile's 128 keys
-    auto emit_k = [&](const TileSrc& ts, int blk) {
-      if (e % C::NPW == pw) {
-        const int sl = claim();
-        if (sl >= 0) {
-          uint8_t* dst = ring + sl * C::CHUNK;
-          if (ts.prefix) {
-            // lane g issues group g's box: the page groups' copies start
-            // together instead of one after another from a single thread
-            if (lane == 0) {
-              int tx = 0;
-#pragma unroll
-              for (int g = 0; g < C::NGRP; ++g)
-                if (by_tma(ts, g)) tx += 2048;
-              slot_cp[sl] = tx == C::NGRP * 2048 ? 0u : 1u;
-              mbar_arrive_expect_tx(&full[sl], tx);
-            }
-            __syncwarp();
-            if (lane < C::NGRP && tma_group(ts, lane, ts.my_row0))
-              tma_load_3d(dst + lane * 2048, &tm_k, &full[sl], 0, blk, ts.my_row0, pol);
-            bool any_cp = false;
-#pragma unroll
-            for (int g = 0; g < C::NGRP; ++g) {
-              if (by_tma(ts, g)) continue;
-              any_cp = true;
-              // 16 rows x 8 units: lane copies rows lane / 8 + 4 i, unit lane % 8;
-              // rows holding no visible key read as zero (stale rows may be NaN)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr;
-                const bool v = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
-                const uint8_t* src =
-                    p.k_slab + (v ? (static_cast<size_t>(ts.row0[g] + rr) * D + blk * 64) * 2 + (lane & 7) * 16 : 0);
-                cp_async16_zfill(dst + sw128(r, lane & 7), src, v, pol);
-              }
-            }
-            if (any_cp) cp_async_mbar_arrive(&full[sl]);
-            else if (lane == 0) mbar_arrive_n(&full[sl], 32);
-          } else {
-            mark(sl, false);
-            if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::CHUNK);
-            __syncwarp();
-            if (lane < 2)   // two 64-row boxes, one per lane
-              tma_load_4d(dst + lane * (C::CHUNK / 2), &tm_kx, &full[sl], 0, blk, x.h, ts.tok0 + 64 * lane, pol);
-            if (lane == 0) mbar_arrive_n(&full[sl], 32);
-          }
-        }
-      }
-      ++e;
-    };
-    // V slot v of a tile: page groups 2v, 2v + 1, each 16 keys x the CTA's
-    // 256 columns ([4 column blocks][16 rows][128 B], 8 KB)
-    auto emit_v = [&](const TileSrc& ts, int v) {
-      if (e % C::NPW == pw) {
-        const int sl = claim();
-        if (sl >= 0) {
-          uint8_t* dst = ring + sl * C::CHUNK;
-          const int blk0 = x.ds * C::NVB;
-          if (ts.prefix) {
-            const int g_l = 2 * v + (lane & 1);   // lanes 0, 1: groups 2v, 2v + 1
-            const int r_l = __shfl_sync(0xffffffffu, ts.my_row0, g_l);
-            if (lane == 0) {
-              int tx = 0;
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                if (by_tma(ts, 2 * v + h)) tx += 8192;
-              slot_cp[sl] = tx == 2 * 8192 ? 0u : 1u;
-              mbar_arrive_expect_tx(&full[sl], tx);
-            }
-            __syncwarp();
-            if (lane < 2 && tma_group(ts, g_l, r_l))
-              tma_load_3d(dst + lane * 8192, &tm_vg, &full[sl], 0, r_l, blk0, pol);
-            bool any_cp = false;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int g = 2 * v + h;
-              if (by_tma(ts, g)) continue;
-              any_cp = true;
-              const int row0 = __shfl_sync(0xffffffffu, ts.my_row0, g);
-              // 4 blocks x 16 rows x 8 units: lane copies units lane + 32 i
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int idx = lane + 32 * i, b = idx >> 7, rr = (idx >> 3) & 15, uu = idx & 7;
-                const int r = 16 * g + rr;
-                const bool ok_row = row0 >= 0 && r < ts.lim && r >= ts.wlim;
-                const uint8_t* src =
-                    p.v_slab + (ok_row ? (static_cast<size_t>(row0 + rr) * D + (blk0 + b) * 64) * 2 + uu * 16 : 0);
-                cp_async16_zfill(dst + h * 8192 + b * 2048 + sw128(rr, uu), src, ok_row, pol);
-              }
-            }
-            if (any_cp) cp_async_mbar_arrive(&full[sl]);
-            else if (lane == 0) mbar_arrive_n(&full[sl], 32);
-          } else {
-            mark(sl, false);
-            if (lane == 0) mbar_arrive_expect_tx(&full[sl], C::CHUNK);
-            __syncwarp();
-            if (lane < 2)   // tokens of groups 2v, 2v + 1
-              tma_load_4d(dst + lane * 8192, &tm_vxg, &full[sl], 0, ts.tok0 + 16 * (2 * v + lane), x.h, blk0, pol);
-            if (lane == 0) mbar_arrive_n(&full[sl], 32);
-          }
-        }
-      }
-      ++e;
-    };
-    PageRef pid_next = load_pid(0);
-    TileSrc src_cur{}, src_prev{};
-    for (int t = 0; ok && t <= nt; ++t) {
-      if (t < nt) {
-        const PageRef pid = pid_next;
-        pid_next = load_pid(t + 1);   // a tile ahead
-        src_cur = tile_src(t, pid);
-        for (int kb = 0; ok && kb < C::KB; ++kb) emit_k(src_cur, kb);
-      }
-      if (t >= 1)
-        for (int v = 0; ok && v < C::NVB; ++v) emit_v(src_prev, v);
-      src_prev = src_cur;
-    }
-    if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-    // drain: no copy may still be landing when the CTA exits
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    if (lane == 0) {
-      for (int i = max(0, e - C::NSLOT); i < e; ++i)
-        if (i % C::NPW == pw && !mbar_wait(&full[i % C::NSLOT], (i / C::NSLOT) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-    }
-    if (threadIdx.x == 0 && !mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-  } else if (warp == C::W_MMA) {
-    // ---------------------------------------------------------- MMA issuer
-    // The whole warp walks the schedule and waits on the barriers; one
-    // elected lane issues the MMAs and the commits that track them.
-    const uint32_t idS = umma_idesc_bf16(C::M, C::NK, false);   // S: N = 128 keys, K-major B
-    const uint32_t idO = umma_idesc_bf16(C::M, C::DS, true);    // PV: N = 256 columns, MN-major B
-    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0) && mbar_wait(qt_full, 0));
-    tc_fence_after();
-    const uint64_t qd0 = umma_desc_sw128(smem_u32(qs), 16, 1024);   // Q's shared-memory blocks
-    const uint64_t pd0 = umma_desc_sw128(smem_u32(ps), 16, 1024);   // P's two key blocks
-    const uint32_t s_tmem = tmem + C::S_COL0;
-    int e = 0;
-    // wait for ring position ee, return its address; a slot that cp.async
-    // filled (partly) is fenced: those generic-proxy writes, seen through the
-    // barrier, are ordered before the MMAs' async-proxy reads
-    auto wait_slot = [&](int ee) -> uint32_t {
-      const int sl = ee % C::NSLOT;
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[sl], (ee / C::NSLOT) & 1));
-      if (slot_cp[sl]) fence_proxy_async_smem();
-      return smem_u32(ring + sl * C::CHUNK);
-    };
-    for (int t = 0; ok && t <= nt; ++t) {
-      if (t < nt) {
-        // S_t overwrites S once every softmax warp holds S_{t-1} in registers
-        if (t >= 1) ok = __all_sync(0xffffffffu, mbar_wait(s_free, (t - 1) & 1));
-        tc_fence_after();
-        for (int kb = 0; ok && kb < C::KB; ++kb) {
-          const uint32_t kaddr = wait_slot(e);
-          if (!ok) break;
-          tc_fence_after();
-          // one descriptor per chunk; a K16 step advances 32 bytes along the
-          // swizzled row (start-address field +2, no carry below 256 KB)
-          const uint64_t kd = umma_desc_sw128(kaddr, 16, 1024);
-          if (elect_one()) {
-            if (kb < C::NQT) {   // A = Q block from tensor memory
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_ts(s_tmem, tmem + C::Q_COL0 + kb * 32 + ks * 8, kd + 2 * ks, idS, (kb > 0 || ks > 0) ? 1u : 0u);
-            } else {             // A = Q block from shared memory
-              const uint64_t qd = qd0 + static_cast<uint64_t>((kb - C::NQT) * (C::M * 128) / 16);
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) umma_ss(s_tmem, qd + 2 * ks, kd + 2 * ks, idS, 1u);
-            }
-            umma_commit(&empty[e % C::NSLOT]);   // the chunk is free once these MMAs complete
-          }
-          __syncwarp();
-          ++e;
-        }
-        if (!ok) break;
-        if (elect_one()) umma_commit(s_full);   // S_t completes phase t of s_full
-        __syncwarp();
-      }
-      if (t >= 1) {
-        const int i = t - 1;
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(p_full, i & 1));   // P_i is in shared memory
-        if (!ok) break;
-        // V_i: NVB chunks in consecutive slots (a group never wraps the ring)
-        uint32_t vaddr = 0;
-        for (int v = 0; ok && v < C::NVB; ++v) {
-          const uint32_t a = wait_slot(e + v);
-          if (v == 0) vaddr = a;
-        }
-        if (!ok) break;
-        tc_fence_after();
-        // V page group ks (8 KB apart) holds keys 16 ks .. 16 ks + 15; its 4
-        // column blocks lie 2 KB apart (LBO), its two 8-key halves 1 KB (SBO)
-        const uint64_t vd0 = umma_desc_sw128(vaddr, 2048, 1024);
-        if (elect_one()) {
-#pragma unroll
-          for (int ks = 0; ks < C::NK / 16; ++ks)
-            umma_ss(tmem, pd0 + static_cast<uint64_t>((ks >> 2) * (C::M * 128) / 16 + 2 * (ks & 3)),
-                    vd0 + static_cast<uint64_t>(ks * 8192 / 16), idO, (i > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-          for (int v = 0; v < C::NVB; ++v) umma_commit(&empty[(e + v) % C::NSLOT]);
-          umma_commit(o_bar);   // PV_i completes phase i of o_bar
-        }
-        __syncwarp();
-        e += C::NVB;
-      }
-    }
-    if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-    // every MMA the elected lane issued has finished before tensor memory is freed
-    if (elect_one()) umma_commit(&done_bar);
-    __syncwarp();
-    if (!__all_sync(0xffffffffu, mbar_wait(&done_bar, 0)) && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-  } else {
-    // ------------------------------------------------------------- softmax
-    // Two warps per row quarter (tensor-memory lane access follows warp % 4):
-    // the first four take columns [0, 64) of each 128-key tile, the other
-    // four [64, 128).  They exchange their tile maxima through shared memory
-    // (rounded up to integers, max_code), keep their own
-    // shares of the denominator, and meet once in the epilogue.
-    __shared__ short sm_mx[2][2][C::M];   // [tile parity][half][row]: max_code values
-    constexpr int SMX_BAR = 2, SMX_THREADS = C::NSMX * 32;
-    constexpr int HC = C::NK / 2;                // score columns per thread
-    bool range_bad = false;
-    const int half = (warp - (C::W_MMA + 1)) >> 2;
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;   // query row = tensor-memory lane
-    const int tl = r / p.g, hj = r % p.g;
-    const int t = x.t0 + tl;
-    const bool row_ok = t < x.n;
-    const int qpos = x.P + t;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    {
-      // this row's first NQT * 64 query values into tensor memory (row =
-      // lane, bf16 pairs per column: the A-operand layout of the S MMA),
-      // half h copying blocks h, h + 2; rows past the last token are zero
-      const int tok = x.qo0 + t;
-      const bool in = tok < p.num_tokens;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
-#pragma unroll 1
-      for (int kb = half; kb < C::NQT; kb += 2) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = in ? __ldg(src + kb * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-        tmem_st32(trow + C::Q_COL0 + kb * 32, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qt_full);
-    }
-    const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
-    const float sc = p.scale_log2;
-    // l_run: this half's share of the denominator, the sum of the bf16
-    // weights the PV MMA uses; l_lse: the sum of the unrounded weights, for lse
-    float m_run = -INFINITY, l_run = 0.f, l_lse = 0.f;
-    bool ok = true, bad = false;
-    constexpr int OH = C::DS / 2;            // O columns this half rescales and writes
-    uint8_t* prow = ps + half * (C::M * 128);   // this half's P block: keys [64 half, 64 half + 64)
-    for (int j = 0; j < nt; ++j) {
-      const int xb = j & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1));
-      const bool pre = x.prefix(j);
-      const int st0 = x.start(j) + HC * half;   // key of this half's first column
-      float sv[HC];
-      float mt = -INFINITY;
-      if (got) {
-        tc_fence_after();
-        uint32_t sa[32], sb[32];
-        tmem_ld32(trow + C::S_COL0 + HC * half, sa);
-        tmem_ld32(trow + C::S_COL0 + HC * half + 32, sb);
-        tmem_ld_wait();
-        // this warp's part of S_j is in registers: S may take S_{j+1}
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
-        const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.Pk - 1) : qpos);
-        const int clo = klo - st0, chi = khi - st0;
-        if (__all_sync(0xffffffffu, clo <= 0 && chi >= HC - 1)) {   // every column visible to the warp's rows
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            sv[c] = __uint_as_float(sa[c]);
-            sv[32 + c] = __uint_as_float(sb[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            sv[c] = (c >= clo && c <= chi) ? __uint_as_float(sa[c]) : -INFINITY;
-            sv[32 + c] = (32 + c >= clo && 32 + c <= chi) ? __uint_as_float(sb[c]) : -INFINITY;
-          }
-        }
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
-#pragma unroll
-        for (int c = 0; c < HC; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
-        const short mr = max_code(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc, range_bad);
-        sm_mx[xb][half][r] = mr;
-        mt = max_decode(mr);
-      }
-      // every warp has published its maximum
-      ok = named_bar_and(SMX_BAR, SMX_THREADS, got && !bad);
-      if (!ok) break;
-      mt = fmaxf(mt, max_decode(sm_mx[xb][half ^ 1][r]));
-      const float m_new = fmaxf(m_run, mt);
-      const bool need = m_new > m_run + 8.0f;   // rescale only when the max grows by more than 2^8
-      const bool resc = need && m_run > -INFINITY;
-      const float f = resc ? ex2(m_run - m_new) : (need ? 0.f : 1.0f);   // this row's factor for O and l
-      if (need) {
-        l_run *= f;
-        l_lse *= f;
-        m_run = m_new;
-      }
-      // the weights first, in registers: only their store and the rescale of O
-      // wait for PV_{j-1}
-      // a row with no visible key so far has m_run = -inf and only -inf scores: exponent base 0 gives 0
-      const float mb = (m_run > -INFINITY) ? m_run : 0.f;
-      float lsum[4] = {0.f, 0.f, 0.f, 0.f}, pe[2] = {0.f, 0.f};
-      uint32_t pk[HC / 2];
-#pragma unroll
-      for (int c = 0; c < HC / 2; ++c) {
-        const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
-        const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
-        pe[c & 1] += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-        // the denominator sums the bf16-rounded weights the PV MMA uses
-        lsum[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
-      }
-      // PV_{j-1} must have completed before O is rescaled and before P_j
-      // overwrites the P that PV_{j-1} reads
-      bool pv_done = true;
-      if (j > 0) {
-        pv_done = __all_sync(0xffffffffu, mbar_wait(o_bar, (j - 1) & 1));
-        if (!pv_done) {
-          bad = true;   // leaves the loop at the next tile's barrier
-          if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-        }
-      }
-      if (pv_done && __any_sync(0xffffffffu, resc) && j > 0) {
-        tc_fence_after();
-        const float fo = resc ? f : 1.0f;
-        // 16 columns at a time: the weights of this tile are live in registers
-#pragma unroll 1
-        for (int c = half * OH; c < (half + 1) * OH; c += 16) {
-          uint32_t o[16];
-          tmem_ld16(trow + c, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * fo);
-          tmem_st16(trow + c, o);
-        }
-        tmem_st_wait();
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)   // 8 keys per 16-byte unit of the P row
-        *reinterpret_cast<uint4*>(prow + sw128(r, u)) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      l_run += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
-      l_lse += pe[0] + pe[1];
-      // the generic P writes, ordered for the PV MMA's async-proxy reads
-      fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
-    bool fin = ok;
-    if (fin && nt > 0) fin = __all_sync(0xffffffffu, mbar_wait(o_bar, (nt - 1) & 1));
-    // every MMA has completed, so every ring slot was consumed: the ring is idle
-    float* sm_l = reinterpret_cast<float*>(ring);   // [half][row]: rounded sums, then unrounded ones
-    if (fin) {
-      sm_l[half * C::M + r] = l_run;
-      sm_l[(2 + half) * C::M + r] = l_lse;
-    }
-    fin = named_bar_and(SMX_BAR, SMX_THREADS, fin);
-    const float l_tot = fin ? l_run + sm_l[(half ^ 1) * C::M + r] : 0.f;
-    const float l_all = fin ? l_lse + sm_l[(2 + (half ^ 1)) * C::M + r] : 0.f;
-    if (!fin) {
-      if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-    } else {
-      tc_fence_after();
-      const float inv = (l_tot > 0.f) ? 1.0f / l_tot : 0.f;
-      __nv_bfloat16* orow =
-          p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS;
-#pragma unroll 1
-      for (int c = half * OH; c < (half + 1) * OH; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(trow + c, o);
-        tmem_ld_wait();
-        if (row_ok) {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            reinterpret_cast<uint4*>(orow + c)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-        }
-      }
-      if (row_ok && half == 0 && x.ds == 0 && p.lse)
-        p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
-            (m_run > -INFINITY && l_all > 0.f) ? (m_run + __log2f(l_all)) * 0.69314718055994531f : -INFINITY;
-    }
-  }
-
-  // ------------------------------------------------------------- teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == C::W_MMA) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
 template <int D, int KV>
 static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStream_t s) {
   using C = ExtCfg<D>;
@@ -1495,29 +865,6 @@ static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStrea
   const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
   return launch_pdl(extend_kernel<D, KV>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
                     a.tm_vx, k);
-}
-
-template <int D>
-static cudaError_t launch_extend128_t(const ExtendArgs& a, const ExtK& k, cudaStream_t s) {
-  using C = E128Cfg<D>;
-  static unsigned int done = 0;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend128_kernel<D>), C::SMEM_ALLOC, &done);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
-  return launch_pdl(extend128_kernel<D>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_vg, a.tm_kx,
-                    a.tm_vxg, k);
-}
-
-// bf16 slabs: head_dim 512 takes the 128-key kernel and head_dim 256 the
-// 64-key one, the faster of the two at each width (both compute the same
-// attention).  FA_EXTEND_TILE=64 or =128 selects one kernel for both widths.
-static int extend_tile(int D) {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("FA_EXTEND_TILE");
-    v = (e && e[0] == '6' && e[1] == '4') ? 64 : (e && e[0] == '1' && e[1] == '2' && e[2] == '8') ? 128 : 0;
-  }
-  return v ? v : (D == 512 ? 128 : 64);
 }
 
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
@@ -1558,9 +905,7 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
     return a.D == 256 ? launch_extend_t<256, FA_KV_INT8>(a, k, s) : launch_extend_t<512, FA_KV_INT8>(a, k, s);
   if (a.kv_dtype == FA_KV_FP8)
     return a.D == 256 ? launch_extend_t<256, FA_KV_FP8>(a, k, s) : launch_extend_t<512, FA_KV_FP8>(a, k, s);
-  if (extend_tile(a.D) == 64)
-    return a.D == 256 ? launch_extend_t<256, FA_KV_BF16>(a, k, s) : launch_extend_t<512, FA_KV_BF16>(a, k, s);
-  return a.D == 256 ? launch_extend128_t<256>(a, k, s) : launch_extend128_t<512>(a, k, s);
+  return a.D == 256 ? launch_extend_t<256, FA_KV_BF16>(a, k, s) : launch_extend_t<512, FA_KV_BF16>(a, k, s);
 }
 
 }  // namespace fa

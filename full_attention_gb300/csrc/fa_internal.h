@@ -32,10 +32,6 @@ struct Slab {
   // boxes of tm_k / tm_v side by side (one copy per tile).
   CUtensorMap tm_kt;
   CUtensorMap tm_vt;
-  // bf16 V as (column-block element, row, column block) with a box of 16
-  // rows x 4 column blocks: one page group of 256 output columns, landing as
-  // 4 consecutive 2 KB pieces of 16 rows x 128 B (extend's V layout).
-  CUtensorMap tm_vg;
   // int8 format: 2-D maps over the fp32 scales, one 16-float box per tile.
   CUtensorMap tm_ks;
   CUtensorMap tm_vs;
@@ -174,7 +170,6 @@ struct ExtendArgs {
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_ks;
   const CUtensorMap* tm_vs;
-  const CUtensorMap* tm_vg;   // the slab's page-group map of V (bf16)
   void* out;
   float* lse;
   int B, Hq, Hkv, D, kind, window, page_size, num_pages, max_pages_per_seq, max_q_len,
@@ -183,9 +178,8 @@ struct ExtendArgs {
   float sm_scale;
   unsigned int* err;
   // per-call maps: q as (64-column block, head, token, block index) boxes of
-  // (64, g, 128/g, 1); k_ext / v_ext as (64, block, KV head, token) boxes of
-  // (64, 1, 1, 64); v_ext as (64, token, KV head, block) boxes of (64, 16, 1, 4)
-  CUtensorMap tm_q, tm_kx, tm_vx, tm_vxg;
+  // (64, g, 128/g, 1); k_ext / v_ext as (64, block, KV head, token) boxes of (64, 1, 1, 64)
+  CUtensorMap tm_q, tm_kx, tm_vx;
 };
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s);
 

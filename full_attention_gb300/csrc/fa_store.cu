@@ -62,13 +62,14 @@ cudaError_t clear_device_error_word(const fa_cache* c) {
 }
 
 // R consecutive (token, KV head, K or V) rows per warp, `warp` counting the
-// launch's warps for this layer.  The warp first loads the R slots, then all
-// R rows (R * D / 256 16-byte vectors per lane in flight), then stores them:
-// with one row per warp the store was bound by the latency of its two
-// dependent loads, not by bandwidth.
+// launch's warps for this layer.  The warp loads the R slots, then (once the
+// previous kernel's rows may be read) all R rows, whose addresses do not
+// depend on the slots, then stores them: R * D / 256 16-byte vectors per lane
+// in flight behind one load latency.  Row t * Hkv * 2 + 2 h (+1) is token t's
+// K (V) row of KV head h.
 template <int D>
 struct StoreShape {
-  static constexpr int R = D == 256 ? 4 : 2;   // rows per warp: 64 bytes per lane in flight
+  static constexpr int R = D == 256 ? 8 : 4;   // rows per warp: 128 bytes per lane in flight
 };
 
 template <int D, int KV>
@@ -77,44 +78,31 @@ __device__ __forceinline__ void store_rows(const StoreArgs& a, int warp, int lan
   const int rows = a.T * a.Hkv * 2;
   const int r0 = warp * R;
   if (r0 >= rows) return;
-  size_t dst[R];
-  bool ok[R];
+  int slot[R];
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int row = r0 + i;
-    ok[i] = false;
-    dst[i] = 0;
-    if (row < rows) {
-      const int th = row >> 1;   // row = 2 * (t * Hkv + h) + (0: K, 1: V)
-      const int t = th / a.Hkv, h = th % a.Hkv;
-      const int slot = __ldg(a.slots + t);
-      if (slot >= 0) {           // a negative slot is a padding token
-        const int page = slot / a.page_size, off = slot % a.page_size;
-        if (page >= a.num_pages) {
-          if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
-        } else {
-          ok[i] = true;
-          dst[i] = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
-        }
-      }
-    }
-  }
+  for (int i = 0; i < R; ++i) slot[i] = (r0 + i < rows) ? __ldg(a.slots + ((r0 + i) >> 1) / a.Hkv) : -1;
   griddep_wait();   // the rows (and the slab) may belong to the previous kernel
   RowRegs<D> r[R];
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int row = r0 + i;
-    if (ok[i])
-      row_load<D>(r[i], static_cast<const __nv_bfloat16*>((row & 1) ? a.v : a.k) + static_cast<size_t>(row >> 1) * D,
-                  lane);
-  }
+  for (int i = 0; i < R; ++i)
+    if (r0 + i < rows)
+      row_load<D>(r[i], static_cast<const __nv_bfloat16*>(((r0 + i) & 1) ? a.v : a.k) +
+                            static_cast<size_t>((r0 + i) >> 1) * D, lane);
   constexpr size_t elem = KV == FA_KV_BF16 ? 2 : 1;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
-    const int which = (r0 + i) & 1;
-    if (ok[i])
-      row_store<D, KV>(r[i], static_cast<uint8_t*>(which ? a.v_slab : a.k_slab) + dst[i] * D * elem,
-                       KV == FA_KV_BF16 ? nullptr : (which ? a.v_scale : a.k_scale) + dst[i], lane);
+    const int row = r0 + i;
+    if (row >= rows || slot[i] < 0) continue;   // a negative slot is a padding token
+    const int page = slot[i] / a.page_size, off = slot[i] % a.page_size;
+    if (page >= a.num_pages) {
+      if (lane == 0) atomicOr(a.err, FA_DEV_ERR_SLOT);
+      continue;
+    }
+    const int h = (row >> 1) % a.Hkv;
+    const size_t dst = (static_cast<size_t>(page) * a.Hkv + h) * a.page_size + off;
+    const int which = row & 1;
+    row_store<D, KV>(r[i], static_cast<uint8_t*>(which ? a.v_slab : a.k_slab) + dst * D * elem,
+                     KV == FA_KV_BF16 ? nullptr : (which ? a.v_scale : a.k_scale) + dst, lane);
   }
 }
 
