@@ -33,11 +33,20 @@
 //               more than 2^8, so rescales are rare; final normalisation and
 //               bf16 store.
 // 8-bit slabs (int8 or fp8 per-token-head codes): every MMA operand is f16.
-// The producers dequantise the prefix rows (code * scale, rounded once to f16)
-// into the same shared-memory layout instead of copying them, and convert the
-// bf16 chunk rows to f16; the softmax warps write Q as f16.  A value f16
-// cannot hold (magnitude 65520 or more) saturates to +-65504 and sets
-// FA_DEV_ERR_RANGE.
+// A loader warp copies each slot as soon as it is free: a prefix slot's raw
+// codes by cp.async into the slot's upper half, a chunk slot's bf16 rows by
+// TMA as in the bf16 path.  The four producer warps then rewrite the slot in
+// place as exact f16 values (int8: a byte permute and one subtraction per
+// pair; e4m3: the hardware pair conversion; chunk rows: bf16 to f16), each
+// taking one 16-row group; the softmax warps write Q as f16.  The per-key scales never touch the
+// operands: producer warp 0 puts each tile's K scale (times the softmax
+// scale) and V scale into a small ring beside the tiles; the softmax
+// multiplies the fp32 scores by the K scale and folds the V scale into P.
+// Its exponent base then tracks the largest score plus the largest log2 V
+// scale of the tile half and sits 2^7 below it, so the weighted P stays
+// below 2^15 whatever the scales.  A q or chunk value f16 cannot hold
+// (magnitude 65520 or more) saturates to +-65504 and sets FA_DEV_ERR_RANGE;
+// stored prefix rows have no such limit.
 // Every wait is bounded; tensor memory is always freed.
 #include <cfloat>
 
@@ -48,7 +57,7 @@
 
 namespace fa {
 
-template <int D>
+template <int D, int KV = FA_KV_BF16>
 struct ExtCfg {
   static constexpr int M = 128;                 // query rows per CTA
   static constexpr int NK = 64;                 // keys per tile
@@ -68,19 +77,34 @@ struct ExtCfg {
   static constexpr int CPS = D == 256 ? 4 : 2;  // chunks (column blocks) per ring slot
   static constexpr int SLOT = CPS * CHUNK;      // one ring slot: CPS chunks side by side
   static constexpr int BAR_BYTES = 1024;
+  // 8-bit slabs: a ring of per-tile key scales, SCL_R tiles deep; per tile
+  // 64 K scales x softmax scale, 64 V scales, and per half of the keys the
+  // largest log2 V scale
+  static constexpr bool Q8 = KV != FA_KV_BF16;
+  static constexpr int SCL_R = 8;
+  static constexpr int SCL_TILE = 3 * 64 * 4;
+  static constexpr int SCL_BYTES = Q8 ? SCL_R * SCL_TILE : 0;
+  // 8-bit slabs: a prefix slot's raw codes (CPS x 64 rows x 64 codes) land
+  // in the slot's upper half, in 128-byte lines of 128 codes
+  static constexpr int CODE_OFF = SLOT / 2;
+  static constexpr int NPW = 4;                 // producer warps
   // the rest of shared memory is a ring of slots; per tile KB K chunks and 4 V blocks pass through it
-  static constexpr int NSLOT = (232448 - 1024 - Q_BYTES - BAR_BYTES) / SLOT;
+  static constexpr int NSLOT = (232448 - 1024 - Q_BYTES - BAR_BYTES - SCL_BYTES) / SLOT;
   static constexpr int OFF_RING = Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT;
-  static constexpr int SMEM = OFF_BAR + BAR_BYTES;
+  static constexpr int OFF_SCL = OFF_BAR + BAR_BYTES;
+  static constexpr int SMEM = OFF_SCL + SCL_BYTES;
   static constexpr int SMEM_ALLOC = SMEM + 1024;
   // 16-row groups 0 .. TMA_GROUPS - 1 of a prefix tile come by TMA, the
   // others by the producer warp's cp.async copies (two copy paths in parallel)
   static constexpr int TMA_GROUPS = 2;
-  static constexpr int NPW = 4;                 // producer warps
   static constexpr int W_MMA = NPW;             // the MMA warp; the softmax warps follow it
   static constexpr int NSMX = 8;                // softmax warps: two per tensor-memory lane quarter
-  static constexpr int NTHR = (NPW + 1 + NSMX) * 32;
+  // 8-bit slabs: one more warp, the loader, issues every slot's TMA copies
+  // (the producer warps convert what lands); an SM sub-partition then holds
+  // 4 warps at most, so the register budget (128) is unchanged
+  static constexpr int W_LOAD = NPW + 1 + NSMX;
+  static constexpr int NTHR = (NPW + 1 + NSMX + (Q8 ? 1 : 0)) * 32;
   // tensor memory columns: O [0, DS), S/P buffers [DS, DS + 64) and
   // [DS + 64, DS + 128), Q blocks 0..NQT-1 [DS + 128, 512) (32 columns of
   // bf16 pairs each)
@@ -89,7 +113,7 @@ struct ExtCfg {
   static constexpr uint32_t Q_COL0 = DS + 128;
   static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static_assert((1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 1) * 8 <= BAR_BYTES, "barrier space");
+  static_assert((1 + 3 * NSLOT + 2 + 2 + 2 + 1 + 1 + 1 + 2 * SCL_R) * 8 <= BAR_BYTES, "barrier space");
   static_assert(NSLOT >= KB / CPS + NVB / CPS, "a ring must hold one tile");
   // a producer warp's consecutive slots lie NPW ring positions apart; its
   // parity wait on a slot's empty barrier is sound only while that is at most
@@ -187,42 +211,34 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   return true;
 }
 
-// 32 consecutive 8-bit codes (two 16-byte words) times the row's scale,
-// rounded once to f16 and packed in pairs (the MMAs over 8-bit slabs run in
-// f16, which keeps 11 significant bits of the dequantised values).  int8 codes
-// are exact in fp32, e4m3 codes exact in f16.
+// 32 consecutive 8-bit codes (two 16-byte words) as exact f16 values, packed
+// in pairs (lower column in the lower half).  int8: with u = c + 128 (the
+// byte xor 0x80), the f16 bit pattern 0x6400 | u is 1024 + u, so one
+// subtraction of 1152 per pair leaves c exactly; e4m3: the hardware pair
+// conversion (every e4m3 value, subnormals included, is an f16 normal).
 template <int KV>
-__device__ __forceinline__ void dequant32(const uint4 (&w)[2], float s, uint32_t (&out)[16]) {
+__device__ __forceinline__ void codes32(const uint4 (&w)[2], uint32_t (&out)[16]) {
   const uint32_t word[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float f[4];
     if constexpr (KV == FA_KV_INT8) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) f[b] = static_cast<float>(static_cast<int8_t>((word[i] >> (8 * b)) & 0xffu));
+      const uint32_t u = word[i] ^ 0x80808080u;
+      const __half2 off = __half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
+      uint32_t lo, hi;
+      asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+      asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+      const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), off);
+      const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), off);
+      out[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
+      out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b);
     } else {
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(word[i] >> (16 * b)), __NV_E4M3);
-        __half2 hh;
-        hh.x = __ushort_as_half(hr.x);
-        hh.y = __ushort_as_half(hr.y);
-        const float2 ff = __half22float2(hh);
-        f[2 * b] = ff.x;
-        f[2 * b + 1] = ff.y;
+        out[2 * i + b] = static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
       }
     }
-    out[2 * i] = pack_f16x2_sat(f[0] * s, f[1] * s);
-    out[2 * i + 1] = pack_f16x2_sat(f[2] * s, f[3] * s);
   }
-}
-
-// A row of 8-bit codes with this scale dequantises to a value f16 cannot hold:
-// its largest code magnitude (127 for int8, 448 for e4m3) times the scale
-// reaches 65520, where f16 rounding would give infinity.
-template <int KV>
-__device__ __forceinline__ bool scale_past_f16(float s) {
-  return fabsf(s) * (KV == FA_KV_INT8 ? 127.0f : 448.0f) >= 65520.0f;
 }
 
 // 32 consecutive bf16 values (four 16-byte words) as f16 pairs (saturating);
@@ -256,11 +272,11 @@ __device__ __forceinline__ short max_code(float m, bool& out_of_range) {
 __device__ __forceinline__ float max_decode(short c) { return c == -32768 ? -INFINITY : static_cast<float>(c); }
 
 template <int D, int KV>
-__global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
+__global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kx,
                   const __grid_constant__ CUtensorMap tm_vx, const ExtK p) {
-  using C = ExtCfg<D>;
+  using C = ExtCfg<D, KV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem;
@@ -274,6 +290,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   uint64_t* qt_full = o_bar + 2;        // the softmax warps have put Q into tensor memory
   uint64_t& done_bar = qt_full[1];      // every MMA has completed (before tensor memory is freed)
   uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(qt_full + 2);
+  uint64_t* sc_full = qt_full + 3;      // 8-bit slabs: [SCL_R] a tile's scales are written
+  uint64_t* sc_empty = sc_full + C::SCL_R;   // [SCL_R] the softmax has read them
+  uint64_t* land = sc_empty + C::SCL_R;      // 8-bit slabs: [NSLOT] a slot's TMA data has landed
+  float* scl = reinterpret_cast<float*>(smem + C::OFF_SCL);   // [SCL_R][3][64]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!p.early_metadata) griddep_wait();
@@ -285,7 +305,9 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(&full[i], 33);   // the filling warp: lane 0's expect_tx + 32 lane arrivals
+      // bf16: the filling warp's lane 0 expect_tx + 32 lane arrivals; 8-bit:
+      // one arrival per converting warp
+      mbar_init(&full[i], C::Q8 ? C::NPW : 33);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -296,6 +318,13 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     mbar_init(&o_bar[1], 1);
     mbar_init(qt_full, C::NSMX);
     mbar_init(&done_bar, 1);
+    if constexpr (C::Q8) {
+      for (int i = 0; i < C::SCL_R; ++i) {
+        mbar_init(&sc_full[i], 32);        // the 32 lanes of producer warp 0
+        mbar_init(&sc_empty[i], C::NSMX);  // one arrival per softmax warp
+      }
+      for (int i = 0; i < C::NSLOT; ++i) mbar_init(&land[i], 32);   // the loader warp's 32 lanes
+    }
     fence_mbar_init();
   }
   if (warp == C::W_MMA) tmem_alloc(&tmem_slot, C::TMEM_COLS);
@@ -305,7 +334,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
   const uint32_t tmem = tmem_slot;
   griddep_wait();   // from here on q, k, v, the slab and the outputs are touched
 
-  if (warp < C::NPW) {
+  if (warp < C::NPW || (C::Q8 && warp == C::W_LOAD)) {
     // ----------------------------------------------------------- producers
     // Emission order = the MMA issuer's consumption order: K_0, then for each
     // t >= 1: K_t (if any) and V_{t-1}.  A slot is one 64-key x 64-column
@@ -319,7 +348,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     // with cp.async, zero-filling rows at or past the prefix end.
     // full[] counts 33 arrivals: lane 0's expect_tx, then 32 lane arrivals
     // (when their cp.async copies land, or at once when there are none).
-    const int pw = warp;
+    const int pw = warp < C::NPW ? warp : C::NPW;   // NPW: the 8-bit loader warp
     const uint64_t pol = l2_policy_evict_last();   // K/V rows are shared by the CTAs of a (sequence, head)
     if (threadIdx.x == 0) {
       if constexpr (KV == FA_KV_BF16) {
@@ -393,8 +422,124 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     };
     int e = 0;
     bool ok = true;
+    // 8-bit slabs: convert slot e (its data has landed) in place and mark it
+    // full.  The four producer warps share every slot: warp pw takes row
+    // group pw (rows 16 pw .. 16 pw + 15), lane (row rr, half cpart) 32
+    // columns of its row per column block h.  Prefix codes of block h sit in
+    // the 128-byte lines of the slot's upper half (128 codes = blocks 2k2,
+    // 2k2 + 1 per line, 16-byte pieces 128-byte swizzled); block h's f16 rows
+    // are written over [h x 8 KB, (h + 1) x 8 KB), which covers code lines of
+    // the same rows: the warp reads all its codes, syncs, then writes.  Rows
+    // that hold no visible key become zero.  Chunk rows (bf16) convert piece
+    // by piece in place; rows past the chunk become zero.
+    auto convert = [&](const TileSrc& q) {
+      const int sl = e % C::NSLOT;
+      ok = __all_sync(0xffffffffu, mbar_wait(&land[sl], (e / C::NSLOT) & 1)) && ok;
+      if (!ok) return;
+      uint8_t* dst = ring + sl * C::SLOT;
+      const int rr = lane >> 1, cpart = lane & 1;
+      const int r = 16 * pw + rr;   // this warp's row group: pw
+      if (q.prefix) {
+        const int row0 = pw == 0 ? q.row0[0] : pw == 1 ? q.row0[1] : pw == 2 ? q.row0[2] : q.row0[3];
+        const bool v = row0 >= 0 && r < q.lim && r >= q.wlim;
+        // every code this lane converts is read before any write (the writes
+        // of the last blocks cover the lines the codes sit in)
+        uint4 w[C::CPS][2];
+#pragma unroll
+        for (int h = 0; h < C::CPS; ++h) {
+          const uint8_t* cb = dst + C::CODE_OFF + (h >> 1) * 8192;
+          const int c0 = (h & 1) * 4 + 2 * cpart;
+          w[h][0] = v ? *reinterpret_cast<const uint4*>(cb + sw128(r, c0)) : make_uint4(0u, 0u, 0u, 0u);
+          w[h][1] = v ? *reinterpret_cast<const uint4*>(cb + sw128(r, c0 + 1)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < C::CPS; ++h) {
+          uint32_t pk[16];
+          codes32<KV>(w[h], pk);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(r, cpart * 4 + u)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      } else {
+        uint32_t big = 0;
+        const bool v = r < q.lim;
+#pragma unroll
+        for (int h = 0; h < C::CPS; ++h) {
+          uint8_t* row = dst + h * C::CHUNK;
+          uint4 w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w[u] = v ? *reinterpret_cast<const uint4*>(row + sw128(r, cpart * 4 + u)) : make_uint4(0u, 0u, 0u, 0u);
+          uint32_t pk[16];
+          big |= bf16_to_f16_32(w, pk);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(row + sw128(r, cpart * 4 + u)) =
+                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+        if (__any_sync(0xffffffffu, big != 0) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
+      }
+      // the generic writes, ordered for the MMA's async-proxy reads; full[]
+      // counts one arrival per converting warp
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[sl]);
+    };
     // one slot: column blocks blk0 .. blk0 + CPS - 1 (8 KB each)
     auto emit = [&](const TileSrc& ts, int blk0, bool is_v) {
+      if constexpr (C::Q8) {
+        // the loader copies every slot once it is empty (so copies run as far
+        // ahead as the ring allows); the producer warps convert it together
+        const int sl = e % C::NSLOT;
+        if (pw == C::NPW) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+          ok = __shfl_sync(0xffffffffu, w, 0) && ok;
+          if (ok) {
+            uint8_t* dst = ring + sl * C::SLOT;
+            if (ts.prefix) {
+              // raw codes in the slot's upper half, by cp.async from all 32
+              // lanes (one issuing thread cannot keep up): per 128-code
+              // block k2 and row group g, 16 rows x 8 pieces of 16 bytes,
+              // 128-byte swizzled; pieces of rows that hold no visible key
+              // are not read (the conversion zeroes those rows).  land[]
+              // counts the 32 lanes' arrivals once their copies land
+              const uint8_t* codes = is_v ? p.v_slab : p.k_slab;
+#pragma unroll
+              for (int k2 = 0; k2 < C::CPS / 2; ++k2)
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  const int rg = ts.row0[g];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr, c = lane & 7;
+                    const bool v = rg >= 0 && r < ts.lim && r >= ts.wlim;
+                    const uint8_t* src = codes + (v ? static_cast<size_t>(rg + rr) * D + (blk0 / 2 + k2) * 128 + c * 16 : 0);
+                    cp_async16_zfill(dst + C::CODE_OFF + k2 * 8192 + sw128(r, c), src, v, pol);
+                  }
+                }
+              cp_async_mbar_arrive(&land[sl]);
+            } else {
+              // chunk rows (bf16), as in the bf16 path: lane 0's expect_tx
+              // and 31 plain arrivals
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&land[sl], C::SLOT);
+                for (int h = 0; h < C::CPS; ++h)
+                  tma_load_4d(dst + h * C::CHUNK, is_v ? &tm_vx : &tm_kx, &land[sl], 0, blk0 + h, x.h, ts.tok0, pol);
+              } else {
+                mbar_arrive(&land[sl]);
+              }
+            }
+          }
+          __syncwarp();
+        } else if (ok) {
+          convert(ts);
+        }
+        ++e;
+        return;
+      }
       if (e % C::NPW == pw) {
         const int sl = e % C::NSLOT;
         bool w = true;
@@ -402,78 +547,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         ok = __shfl_sync(0xffffffffu, w, 0) && ok;
         if (ok) {
           uint8_t* dst = ring + sl * C::SLOT;
-          if constexpr (KV != FA_KV_BF16) {
-            if (ts.prefix) {
-              // 8-bit slab: lane (row rr, half cpart) dequantises 32 codes of
-              // one row per (group, column block) into the bf16 layout the TMA
-              // boxes would give; rows that hold no visible key read as zero
-              const uint8_t* codes = is_v ? p.v_slab : p.k_slab;
-              const float* scl = is_v ? p.v_scale : p.k_scale;
-              const int rr = lane >> 1, cpart = lane & 1;
-              float s4[4];
-              bool v4[4], big = false;
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                const int r = 16 * g + rr;
-                v4[g] = ts.row0[g] >= 0 && r < ts.lim && r >= ts.wlim;
-                s4[g] = v4[g] ? __ldg(scl + (v4[g] ? ts.row0[g] + rr : 0)) : 0.f;
-                big |= scale_past_f16<KV>(s4[g]);
-              }
-              if (__any_sync(0xffffffffu, big) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
-#pragma unroll 1
-              for (int h = 0; h < C::CPS; ++h) {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                  const uint4* src = reinterpret_cast<const uint4*>(
-                      codes + static_cast<size_t>(v4[g] ? ts.row0[g] + rr : 0) * D + (blk0 + h) * 64 + cpart * 32);
-                  uint4 w[2];
-                  w[0] = v4[g] ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
-                  w[1] = v4[g] ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
-                  uint32_t pk[16];
-                  dequant32<KV>(w, s4[g], pk);
-#pragma unroll
-                  for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(16 * g + rr, cpart * 4 + u)) =
-                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
-              }
-              // the generic writes, ordered for the MMA's async-proxy reads;
-              // full[] counts lane 0's (empty) expect_tx and 32 lane arrivals
-              fence_proxy_async_smem();
-              if (lane == 0) mbar_arrive_expect_tx(&full[sl], 0);
-              mbar_arrive(&full[sl]);
-            } else {
-              // chunk K and V rows (bf16) as f16 for the MMAs; rows past the
-              // chunk read as zero
-              const uint8_t* ext = is_v ? p.v_ext : p.k_ext;
-              const int rr = lane >> 1, cpart = lane & 1;
-              uint32_t big = 0;
-#pragma unroll 1
-              for (int h = 0; h < C::CPS; ++h) {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                  const int r = 16 * g + rr;
-                  const bool v = r < ts.lim;
-                  const uint4* src = reinterpret_cast<const uint4*>(
-                      ext + ((static_cast<size_t>(v ? ts.tok0 + r : 0) * p.Hkv + x.h) * D + (blk0 + h) * 64 +
-                             cpart * 32) * 2);
-                  uint4 w[4];
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) w[i] = v ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
-                  uint32_t pk[16];
-                  big |= bf16_to_f16_32(w, pk);
-#pragma unroll
-                  for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4*>(dst + h * C::CHUNK + sw128(r, cpart * 4 + u)) =
-                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
-              }
-              if (__any_sync(0xffffffffu, big != 0) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
-              fence_proxy_async_smem();
-              if (lane == 0) mbar_arrive_expect_tx(&full[sl], 0);
-              mbar_arrive(&full[sl]);
-            }
-          } else if (ts.prefix) {
+          if (ts.prefix) {
             if (lane == 0) {
               int tx = 0;
 #pragma unroll
@@ -524,6 +598,55 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       }
       ++e;
     };
+    // 8-bit slabs: warp 0 writes tile t's 64 key scales into scale slot
+    // t % SCL_R once the softmax has released that slot's previous tile: lane
+    // l handles keys l and l + 32.  ck = K scale x softmax scale (log2
+    // domain), cv = V scale; a chunk key (bf16, as is) has ck = softmax scale
+    // and cv = 1, a key that holds nothing visible ck = cv = 0.  Only warp 0
+    // writes, tile by tile, so its parity wait on a slot's empty barrier is
+    // never more than one lap behind; it never waits on anything that needs
+    // the softmax of tile t or later before writing tile t's scales; and
+    // before it waits for the softmax of tile t - SCL_R it converts every
+    // slot it still holds, so that softmax never waits on this warp.
+    float sk0 = 0.f, sk1 = 0.f, sv0 = 0.f, sv1 = 0.f;   // keys lane and lane + 32
+    // key r of the tile lies in row group r / 16, whose slab row is row0
+    auto scale_pair = [&](const TileSrc& ts, int r, int row0, float& k, float& v) {
+      k = v = 0.f;
+      if (ts.prefix) {
+        if (row0 >= 0 && r < ts.lim && r >= ts.wlim) {
+          const int row = row0 + (r & 15);
+          k = __ldg(p.k_scale + row) * p.scale_log2;
+          v = __ldg(p.v_scale + row);
+        }
+      } else if (r < ts.lim) {
+        k = p.scale_log2;
+        v = 1.0f;
+      }
+    };
+    auto write_scales = [&](int t) {
+      const int s = t % C::SCL_R;
+      const uint32_t par = ((t / C::SCL_R) & 1) ^ 1;
+      bool w = mbar_wait(&sc_empty[s], par);
+      ok = __all_sync(0xffffffffu, w) && ok;
+      if (!ok) return;
+      float* dst = scl + s * (C::SCL_TILE / 4);
+      dst[lane] = sk0;
+      dst[lane + 32] = sk1;
+      dst[64 + lane] = sv0;
+      dst[96 + lane] = sv1;
+      // the largest log2 V scale of each half's 32 keys: it only places the
+      // exponent base, held at -90 or more so that the weights of keys with
+      // tiny V scales (2^(score - base) < 2^105) and their sums stay finite
+      float l0 = sv0 > 0.f ? fmaxf(__log2f(sv0), -90.f) : -INFINITY;
+      float l1 = sv1 > 0.f ? fmaxf(__log2f(sv1), -90.f) : -INFINITY;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        l0 = fmaxf(l0, __shfl_xor_sync(0xffffffffu, l0, o));
+        l1 = fmaxf(l1, __shfl_xor_sync(0xffffffffu, l1, o));
+      }
+      if (lane < 2) dst[128 + lane] = lane == 0 ? l0 : l1;
+      mbar_arrive(&sc_full[s]);
+    };
     PageRef pid_next = load_pid(0);
     TileSrc src_cur{}, src_prev{};
     for (int t = 0; ok && t <= nt; ++t) {
@@ -531,18 +654,29 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         const PageRef pid = pid_next;
         pid_next = load_pid(t + 1);   // a tile ahead
         src_cur = tile_src(t, pid);
+        if constexpr (C::Q8)
+          if (pw == 0) {
+            const bool hi = lane >= 16;
+            scale_pair(src_cur, lane, hi ? src_cur.row0[1] : src_cur.row0[0], sk0, sv0);
+            scale_pair(src_cur, lane + 32, hi ? src_cur.row0[3] : src_cur.row0[2], sk1, sv1);
+          }
         for (int kb = 0; ok && kb < C::KB; kb += C::CPS) emit(src_cur, kb, false);
+        if constexpr (C::Q8)
+          if (pw == 0 && ok) write_scales(t);
       }
       if (t >= 1)
         for (int i4 = 0; ok && i4 < C::NVB; i4 += C::CPS) emit(src_prev, x.ds * C::NVB + i4, true);
       src_prev = src_cur;
     }
     if (!ok && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-    // drain: no copy may still be landing when the CTA exits
+    // drain: no copy may still be landing when the CTA exits (8-bit slabs:
+    // the loader waits for its copies, the converting warps issued none)
     asm volatile("cp.async.wait_all;" ::: "memory");
-    if (lane == 0) {
+    if (lane == 0 && (!C::Q8 || pw == C::NPW)) {
       for (int i = max(0, e - C::NSLOT); i < e; ++i)
-        if (i % C::NPW == pw && !mbar_wait(&full[i % C::NSLOT], (i / C::NSLOT) & 1)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+        if ((C::Q8 || i % C::NPW == pw) &&
+            !mbar_wait(C::Q8 ? &land[i % C::NSLOT] : &full[i % C::NSLOT], (i / C::NSLOT) & 1))
+          atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     }
     if (threadIdx.x == 0 && !mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
   } else if (warp == C::W_MMA) {
@@ -708,15 +842,27 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
     const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
     const float sc = p.scale_log2;
     // l_run: this half's share of the denominator, the sum of the rounded
-    // weights the PV MMA uses (so constant V gives exactly that constant);
-    // l_lse: the same sum of the unrounded weights, for lse
+    // weights the PV MMA uses (so constant V gives exactly that constant;
+    // 8-bit slabs: of the unrounded weights, the V scale being folded in);
+    // l_lse: the sum of the unrounded weights, for lse
     float m_run = -INFINITY, l_run = 0.f, l_lse = 0.f;
+    // 8-bit slabs: the exponent base sits 2^7 below the running maximum of
+    // score + the half's largest log2 cv, so the weighted P stays below 2^15
+    constexpr float MB_OFF = C::Q8 ? 7.0f : 0.0f;
     bool ok = true, bad = false;
     constexpr int OH = C::DS / 2;            // O columns this half rescales and writes
+    // 8-bit slabs: per tile the scale slot holds ck (multiplies the raw
+    // scores) and cv (multiplies the weights) of the 64 keys, and per half of
+    // them the largest log2 cv, which joins the maximum
     for (int j = 0; j < nt; ++j) {
       const int sb = j & 1;
       const uint32_t s_col = C::S_COL0 + sb * 64;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (j >> 1) & 1));
+      bool got = mbar_wait(&s_full[sb], (j >> 1) & 1);
+      if constexpr (C::Q8) got = mbar_wait(&sc_full[j % C::SCL_R], (j / C::SCL_R) & 1) && got;
+      got = __all_sync(0xffffffffu, got);
+      const float* sslot = scl + (j % C::SCL_R) * (C::SCL_TILE / 4);
+      const float* ck = sslot + 32 * half;   // this half's 32 keys
+      const float* cvh = sslot + 64 + 32 * half;
       const bool pre = x.prefix(j);
       const int st0 = x.start(j) + 32 * half;   // key of this half's first column
       // raw scores of this row's visible keys (one interval [clo, chi] per
@@ -731,7 +877,21 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         tmem_ld_wait();
         const int khi = !row_ok ? -(1 << 30) : (pre ? min(qpos, x.Pk - 1) : qpos);
         const int clo = klo - st0, chi = khi - st0;
-        if (__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {   // all 32 columns visible to the warp's rows
+        if constexpr (C::Q8) {
+          // scaled scores (log2 domain)
+          const bool all = __all_sync(0xffffffffu, clo <= 0 && chi >= 31);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ck + 4 * c4);
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              const float t = __uint_as_float(sr[c]) * kk[e];
+              sv[c] = (all || (c >= clo && c <= chi)) ? t : -INFINITY;
+            }
+          }
+        } else if (__all_sync(0xffffffffu, clo <= 0 && chi >= 31)) {   // all 32 columns visible to the warp's rows
 #pragma unroll
           for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(sr[c]);
         } else {
@@ -741,7 +901,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four chains, then a tree
 #pragma unroll
         for (int c = 0; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
-        const short mr = max_code(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc, range_bad);
+        const float mxa = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // 8-bit slabs: plus the half's largest log2 V scale, a bound on
+        // score + log2 cv over its keys
+        const short mr = max_code(C::Q8 ? mxa + sslot[128 + half] : mxa * sc, range_bad);
         sm_mx[sb][half][r] = mr;
         mt = max_decode(mr);
       }
@@ -781,30 +944,42 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       uint32_t pk[16];
       float ps[4] = {0.f, 0.f, 0.f, 0.f}, pe[2] = {0.f, 0.f};
       // a row with no visible key so far has m_run = -inf and only -inf scores: exponent base 0 gives 0
-      const float mb = (m_run > -INFINITY) ? m_run : 0.f;
+      const float mb = (m_run > -INFINITY) ? m_run - MB_OFF : 0.f;
+      if constexpr (C::Q8) {
+        // weight q = 2^(score - mb) into the denominator; q x cv, below 2^15
+        // (score + log2 cv <= m_run + 8), into the PV MMA as f16
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
-        const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
-        pe[c & 1] += p0 + p1;
-        // the denominator sums the rounded weights the PV MMA uses (bf16, or
-        // f16 for 8-bit slabs)
-        if constexpr (KV == FA_KV_BF16) {
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(cvh + 4 * c4);
+          const float q0 = ex2(sv[4 * c4] - mb), q1 = ex2(sv[4 * c4 + 1] - mb);
+          const float q2 = ex2(sv[4 * c4 + 2] - mb), q3 = ex2(sv[4 * c4 + 3] - mb);
+          pe[0] += q0 + q1;
+          pe[1] += q2 + q3;
+          pk[2 * c4] = pack_f16x2(q0 * v4.x, q1 * v4.y);
+          pk[2 * c4 + 1] = pack_f16x2(q2 * v4.z, q3 * v4.w);
+        }
+        l_run += pe[0] + pe[1];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = ex2(fmaf(sv[2 * c], sc, -mb));
+          const float p1 = ex2(fmaf(sv[2 * c + 1], sc, -mb));
+          pe[c & 1] += p0 + p1;
+          // the denominator sums the rounded weights the PV MMA uses
           pk[c] = pack_bf16x2(p0, p1);
           ps[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
-        } else {
-          pk[c] = pack_f16x2(p0, p1);
-          const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pk[c]));
-          ps[c & 3] += pf.x + pf.y;
         }
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       }
-      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       l_lse += pe[0] + pe[1];
-      tmem_st16(trow + s_col + 16 * half, pk);   // P of keys [32 half, 32 half + 32): 16 columns of bf16 pairs
+      tmem_st16(trow + s_col + 16 * half, pk);   // P of keys [32 half, 32 half + 32): 16 columns of 16-bit pairs
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (lane == 0) {
+        mbar_arrive(&p_full[sb]);
+        if constexpr (C::Q8) mbar_arrive(&sc_empty[j % C::SCL_R]);   // this tile's scales are read
+      }
     }
     // ------------------------------------------------------------ epilogue
     if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
@@ -843,7 +1018,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
       }
       if (row_ok && half == 0 && x.ds == 0 && p.lse)
         p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
-            (m_run > -INFINITY && l_all > 0.f) ? (m_run + __log2f(l_all)) * 0.69314718055994531f : -INFINITY;
+            (m_run > -INFINITY && l_all > 0.f) ? (m_run - MB_OFF + __log2f(l_all)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -858,7 +1033,7 @@ __global__ void __launch_bounds__(ExtCfg<D>::NTHR, 1)
 
 template <int D, int KV>
 static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStream_t s) {
-  using C = ExtCfg<D>;
+  using C = ExtCfg<D, KV>;
   static unsigned int done = 0;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend_kernel<D, KV>), C::SMEM_ALLOC, &done);
   if (e != cudaSuccess) return e;

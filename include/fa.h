@@ -103,10 +103,11 @@ typedef enum { FA_FULL = 0, FA_SLIDING = 1 } fa_layer_kind;
 #define FA_DEV_ERR_TIMEOUT 0x8u    /* a bounded barrier wait ran out                */
 #define FA_DEV_ERR_WORKSPACE 0x10u /* decode workspace counters were not zero      */
 #define FA_DEV_ERR_RANGE 0x20u     /* a value out of the kernels' range: an f16
-                                      operand saturated (8-bit formats: a q, k or v
-                                      magnitude of 65520 or more), or an extend
-                                      score with |sm_scale * q.k| * log2(e) of
-                                      32767 or more                                 */
+                                      operand saturated (8-bit formats: a q, or
+                                      an extend k_ext / v_ext, magnitude of 65520
+                                      or more), or an extend score with
+                                      |sm_scale * q.k| * log2(e) of 32767 or
+                                      more                                          */
 
 /* Most fa_cache descriptors that may be live at once (each holds one device
  * error word). */
@@ -357,19 +358,17 @@ FA_API fa_status fa_paged_decode_attn_noalloc(fa_cache* cache, int32_t layer, co
  * capacity parameter).  Sequence b has prefix_lens[b] = P_b tokens already
  * in the cache and n_b = qo_indptr[b+1] - qo_indptr[b] new tokens; new token
  * i sits at position P_b + i and attends to prefix positions (from the slab;
- * in the 8-bit formats dequantised as code * scale) and chunk positions
- * P_b + j, j <= i (from k_ext / v_ext, bf16, never quantised), under the
- * layer's mask.  Over 8-bit slabs every tensor-core operand (q, the
- * dequantised and the chunk k, v, and the softmax weights) is f16, with fp32
- * accumulation.  Range: a q, k_ext or v_ext element of magnitude 65536 or
- * more (bf16 has nothing between 65280 and 65536, f16 nothing past 65504),
- * or a prefix row whose largest dequantised magnitude (127 or 448 times its
- * scale) reaches 65520, saturates to +-65504 and sets FA_DEV_ERR_RANGE; the
- * output is then not the exact attention.  At the small end, dequantised
- * values below f16's smallest normal (6.1e-5) are kept as f16 subnormals in
- * steps of 2^-24 (6e-8): rows whose largest magnitude is above about 1e-4
- * keep the stated float tolerance; much smaller rows lose relative accuracy
- * without an error bit.  Every slab format: a scaled score |sm_scale * q.k|
+ * in the 8-bit formats code * scale) and chunk positions P_b + j, j <= i
+ * (from k_ext / v_ext, bf16, never quantised), under the layer's mask.  Over
+ * 8-bit slabs every tensor-core operand is f16 with fp32 accumulation: q,
+ * the chunk k, v, the prefix codes (exact in f16), and the softmax weights
+ * times the keys' V scales; the K scales multiply the fp32 scores.  Range: a
+ * q, k_ext or v_ext element of magnitude 65536 or more (bf16 has nothing
+ * between 65280 and 65536, f16 nothing past 65504) saturates to +-65504 and
+ * sets FA_DEV_ERR_RANGE; the output is then not the exact attention.  Stored
+ * prefix rows have no such limit, and their small magnitudes keep full
+ * relative accuracy; chunk values below f16's smallest normal (6.1e-5) are
+ * kept as f16 subnormals in steps of 2^-24.  Every slab format: a scaled score |sm_scale * q.k|
  * of 32767 / log2(e) (about 22700) or more is out of range (FA_DEV_ERR_RANGE;
  * the two softmax halves of a row agree on an integer base, kept in 16 bits).
  * q: bf16 [N][Hq][D], k_ext, v_ext: bf16 [N][Hkv][D] with N = qo_indptr[B]
@@ -404,7 +403,7 @@ FA_API fa_status fa_paged_extend_attn(fa_cache* cache, int32_t layer, const void
  * lengths including the new tokens, <= max_seq_len; a length below n_b sets
  * FA_DEV_ERR_BOUND), block_table: int32 [B][max_pages_per_seq].  out: bf16
  * [num_tokens][Hq][D]; lse: optional float [num_tokens][Hq].  Every slab
- * format (8-bit keys dequantised as in extend); Hq / Hkv must divide 128. */
+ * format (8-bit codes and scales applied as in extend); Hq / Hkv must divide 128. */
 FA_API fa_status fa_paged_decode_multi_attn(fa_cache* cache, int32_t layer, const void* q, const int32_t* qo_indptr,
                                             const int32_t* seq_lens, const int32_t* block_table,
                                             int32_t max_pages_per_seq, int32_t B, int32_t num_tokens,

@@ -237,9 +237,10 @@ def test_8bit_chunked_prefill_workload(kv_dtype):
 @pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
 @pytest.mark.parametrize("mag", [1e-3, 1e-4], ids=["1e-3", "1e-4"])
 def test_8bit_extend_small_magnitudes(mag, kv_dtype):
-    """Rows of small magnitude: dequantised values (and chunk values) fall
-    below f16's smallest normal number (6.1e-5) and are kept as f16
-    subnormals; rows down to about 1e-4 stay within the float tolerance."""
+    """Rows of small magnitude: the prefix codes enter the MMAs exactly and
+    their scales multiply in fp32, so only the chunk rows (bf16 as f16, some
+    elements f16 subnormals) and the f16 weights round; the relative L2 error
+    stays within the float tolerance."""
     for layer in (lay(W.SLIDING, 256, 8, 2, 64), lay(W.FULL, 512, 8, 1)):
         c = Case8([layer], [70, 150], [90, 33], kv_dtype, seed=35, mag=mag)
         _check(c.extend(0), c.oracle_extend(0), f"small rows x{mag}")
@@ -255,8 +256,8 @@ def test_8bit_extend_f16_range_inside(kv_dtype):
     them in a chunk key row and a stored prefix key row the result also
     matches the oracle: those keys win or lose their softmax rows by
     thousands, a well-conditioned case.  A q element that large is not
-    compared: its scores against the other (dequantised, f16-rounded) keys
-    are about 4000 times the key values, so a rounding of one part in 2^12
+    compared: its scores against the other keys are about 4000 times the
+    key values, so a rounding of one part in 2^12 in the f16 chunk keys
     moves them by several units and the softmax weights with them, on any
     f16 path.  q, V and the prefix V rows are checked for the error bit."""
     def poke_k(kp, vp):
@@ -276,16 +277,12 @@ def test_8bit_extend_f16_range_inside(kv_dtype):
 
 
 @pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
-@pytest.mark.parametrize("where", ["q", "k_ext", "v_ext", "prefix_k", "prefix_v"])
+@pytest.mark.parametrize("where", ["q", "k_ext", "v_ext"])
 def test_8bit_extend_f16_range_outside_sets_error_bit(where, kv_dtype):
-    """A value of 65536, just past the f16 range, in q, in a chunk row or in
-    a stored prefix row: the kernel saturates it and sets FA_DEV_ERR_RANGE."""
-    def poke(kp, vp):
-        if where == "prefix_k":
-            kp[3, 0, 5] = BIG_OUT
-        if where == "prefix_v":
-            vp[7, 0, 9] = -BIG_OUT
-    c = Case8([lay(W.FULL, 256, 4, 1)], [40, 20], [30, 10], kv_dtype, seed=37, poke=poke)
+    """A value of 65536, just past the f16 range, in q or in a chunk row
+    (the values the kernel converts to f16): it saturates and sets
+    FA_DEV_ERR_RANGE."""
+    c = Case8([lay(W.FULL, 256, 4, 1)], [40, 20], [30, 10], kv_dtype, seed=37)
     if where == "q":
         c.q[0][4, 1, 11] = BIG_OUT
     if where == "k_ext":
@@ -294,6 +291,32 @@ def test_8bit_extend_f16_range_outside_sets_error_bit(where, kv_dtype):
         c.vx[0][5, 0, 7] = BIG_OUT
     c.extend(0)
     assert c.fa.device_error() == c.fa.DEV_ERR_RANGE
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+@pytest.mark.parametrize("where", ["prefix_k", "prefix_v"])
+def test_8bit_extend_large_prefix_rows(where, kv_dtype):
+    """Stored prefix rows have no f16 limit: their codes enter the MMAs as
+    exact f16 values and their scales apply in fp32 (K to the scores, V to
+    the weights).  A key element of 65536 keeps parity with the oracle (the
+    key wins or loses its rows by thousands); V elements of -65536 and 3e7
+    (a V scale past f16's range in both formats) match it to the output's
+    bf16 precision, relative to the largest output.  No error bit is set."""
+    def poke(kp, vp):
+        if where == "prefix_k":
+            kp[3, 0, 5] = BIG_OUT
+        else:
+            vp[7, 0, 9] = -BIG_OUT
+            vp[21, 0, 30] = 3.0e7
+    for layer in (lay(W.FULL, 256, 4, 1), lay(W.SLIDING, 512, 8, 2, 40)):
+        c = Case8([layer], [40, 20], [30, 10], kv_dtype, seed=37, poke=poke)
+        out, lse = c.extend(0)
+        ref_out, ref_lse = c.oracle_extend(0)
+        scale = max(1.0, float(np.abs(ref_out).max()))
+        assert_close(out, ref_out, atol=1e-2 * scale, what=f"{where} large")
+        g = lse.double().cpu().numpy()
+        assert np.all(np.abs(g - ref_lse) <= 2e-3 * np.maximum(1.0, np.abs(ref_lse))), f"{where}: lse"
+        assert c.fa.device_error() == 0
 
 
 @pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
