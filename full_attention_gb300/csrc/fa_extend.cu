@@ -34,8 +34,8 @@
 //               bf16 store.
 // 8-bit slabs (int8 or fp8 per-token-head codes): every MMA operand is f16.
 // A loader warp copies each slot as soon as it is free: a prefix slot's raw
-// codes by cp.async into the slot's upper half, a chunk slot's bf16 rows by
-// TMA as in the bf16 path.  The four producer warps then rewrite the slot in
+// codes by TMA into the slot's upper half, a chunk slot's bf16 rows by TMA
+// as in the bf16 path.  The four producer warps then rewrite the slot in
 // place as exact f16 values (int8: a byte permute and one subtraction per
 // pair; e4m3: the hardware pair conversion; chunk rows: bf16 to f16), each
 // taking one 16-row group; the softmax warps write Q as f16.  The per-key scales never touch the
@@ -500,27 +500,30 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
           if (ok) {
             uint8_t* dst = ring + sl * C::SLOT;
             if (ts.prefix) {
-              // raw codes in the slot's upper half, by cp.async from all 32
-              // lanes (one issuing thread cannot keep up): per 128-code
-              // block k2 and row group g, 16 rows x 8 pieces of 16 bytes,
-              // 128-byte swizzled; pieces of rows that hold no visible key
-              // are not read (the conversion zeroes those rows).  land[]
-              // counts the 32 lanes' arrivals once their copies land
-              const uint8_t* codes = is_v ? p.v_slab : p.k_slab;
+              // raw codes in the slot's upper half: TMA boxes of 16 rows x
+              // 128 codes (128-byte swizzled), issued by lanes 0-3, one row
+              // group each, for the groups that hold a readable key (the
+              // conversion zeroes the other rows).  land[] counts lane 0's
+              // expect_tx and 31 plain arrivals, then the bytes
+              if (lane == 0) {
+                int tx = 0;
 #pragma unroll
-              for (int k2 = 0; k2 < C::CPS / 2; ++k2)
+                for (int g = 0; g < 4; ++g)
+                  if (ts.row0[g] >= 0 && 16 * g < ts.lim && 16 * g + 16 > ts.wlim) tx += (C::CPS / 2) * 2048;
+                mbar_arrive_expect_tx(&land[sl], tx);
+              } else {
+                mbar_arrive(&land[sl]);
+              }
+              __syncwarp();
+              if (lane < 4) {
+                const int g = lane;
+                const int rg = g == 0 ? ts.row0[0] : g == 1 ? ts.row0[1] : g == 2 ? ts.row0[2] : ts.row0[3];
+                if (rg >= 0 && 16 * g < ts.lim && 16 * g + 16 > ts.wlim)
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                  const int rg = ts.row0[g];
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    const int rr = (lane >> 3) + 4 * i, r = 16 * g + rr, c = lane & 7;
-                    const bool v = rg >= 0 && r < ts.lim && r >= ts.wlim;
-                    const uint8_t* src = codes + (v ? static_cast<size_t>(rg + rr) * D + (blk0 / 2 + k2) * 128 + c * 16 : 0);
-                    cp_async16_zfill(dst + C::CODE_OFF + k2 * 8192 + sw128(r, c), src, v, pol);
-                  }
-                }
-              cp_async_mbar_arrive(&land[sl]);
+                  for (int k2 = 0; k2 < C::CPS / 2; ++k2)
+                    tma_load_3d(dst + C::CODE_OFF + k2 * 8192 + g * 2048, is_v ? &tm_v : &tm_k, &land[sl], 0,
+                                blk0 / 2 + k2, rg, pol);
+              }
             } else {
               // chunk rows (bf16), as in the bf16 path: lane 0's expect_tx
               // and 31 plain arrivals
