@@ -760,17 +760,21 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         const float alpha = (m_run == -INFINITY) ? 0.0f : ex2(m_run - m_new);
         float psum = 0.0f;
         uint32_t pf[C::NT][2];
-        float vmax = 1.0f;
+        float vmax = 1.0f, ivm = 1.0f;
+        float vsc[C::NT][4];   // 8-bit: this lane's keys' V scales (0 where not visible)
         if constexpr (KV) {
           float vm = 0.0f;
 #pragma unroll
           for (int t = 0; t < C::NT; ++t)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (valid[t][e]) vm = fmaxf(vm, scl[(C::NT + t) * 32 + 2 * tig + (e & 1) + (e >> 1) * 8]);
+            for (int e = 0; e < 4; ++e) {
+              vsc[t][e] = valid[t][e] ? scl[(C::NT + t) * 32 + 2 * tig + (e & 1) + (e >> 1) * 8] : 0.0f;
+              vm = fmaxf(vm, vsc[t][e]);
+            }
           vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 1));
           vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, 2));
           vmax = vm > 0.0f ? vm : 1.0f;
+          ivm = __frcp_rn(vmax);   // one reciprocal per step instead of a division per weight
         }
 #pragma unroll
         for (int t = 0; t < C::NT; ++t) {
@@ -780,8 +784,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
             pe[e] = ex2(s[t][e] - m_new);
             if constexpr (KV) {
               psum += pe[e];
-              const float vsc = scl[(C::NT + t) * 32 + 2 * tig + (e & 1) + (e >> 1) * 8];
-              pe[e] = valid[t][e] ? pe[e] * __fdividef(vsc, vmax) : 0.0f;
+              pe[e] *= vsc[t][e] * ivm;
             }
           }
           if constexpr (!KV) {
@@ -800,7 +803,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* tm_k, const CUten
         m_run = m_new;
         float ofac = alpha;
         if constexpr (KV) {
-          ofac = alpha * __fdividef(sigma, vmax);
+          ofac = alpha * sigma * ivm;
           sigma = vmax;
         }
         // rescale O: this lane's O columns are heads 2tig and 2tig+1
