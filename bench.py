@@ -713,6 +713,10 @@ class PrefillStep:
         plan = W.plan_pages(lens, w.page_size, w.seed)
         self.cache = fa.Cache(w.layers, plan.num_pages, w.page_size, w.kv_dtype)
         self.cache.set_flags(fa.FLAG_EARLY_METADATA)
+        # the extend split workspace: a launch whose last wave would leave
+        # more than half of the SMs idle runs that wave's jobs as two CTAs each
+        self.split_ws = fa.workspace(fa.extend_workspace_bytes(), device)
+        self.cache.bind_extend_workspace(self.split_ws)
         self.slabs = self.cache.allocate(device)
         for k, v, _, _ in self.slabs.values():
             k.zero_()
@@ -776,7 +780,7 @@ class PrefillStep:
                 if events is not None:
                     events[c][li][0].record()
                 out = self.out[li] if outs is None else outs[c][li]
-                self.cache.extend(li, q, k, v, indptr, prefix, self.bt, C, self.nchunks * C, out)
+                self.cache.extend(li, q, k, v, indptr, prefix, self.bt, C, c * C, out)
                 if events is not None:
                     events[c][li][1].record()
             if per_chunk is not None:
@@ -881,7 +885,9 @@ def prefill_measure(args, dev):
                         "algorithmic_flop_per_launch": round(step.total_flops / (step.nchunks * nl)),
                         "per_layer": per_layer},
            "store": store,
-           "gpu_launches_per_prefill": step.launches(), "graph": g_plain is not None}
+           "gpu_launches_per_prefill": step.launches(), "graph": g_plain is not None,
+           "extend_split": "workspace bound: a launch whose last wave would fill at most half of the SMs "
+                           "runs that wave's jobs as two CTAs each (head_dim 512: 56 of 512 jobs on 152 SMs)"}
     res["e2e"] = e2e_prefill(step, args, torch, flush)
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = prefill_cpu_baseline(w, args.cpu_seconds)

@@ -23,6 +23,7 @@ DEV_ERR_PAGE, DEV_ERR_SLOT, DEV_ERR_BOUND, DEV_ERR_TIMEOUT, DEV_ERR_WORKSPACE, D
 MAX_CACHES = 4096
 
 FLAG_EARLY_METADATA = 1
+FLAG_EXTEND_SPLIT_ALL = 2
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
 MAX_LAYERS_PER_LAUNCH = 16
@@ -58,6 +59,8 @@ def _load() -> ctypes.CDLL:
         "fa_kv_bytes_per_token": (sz, [vp, i32]),
         "fa_kv_store": (i32, [vp, i32, vp, vp, vp, i32, vp]),
         "fa_decode_workspace_bytes": (sz, [vp, i32, i32, i32]),
+        "fa_extend_workspace_bytes": (sz, []),
+        "fa_cache_bind_extend_workspace": (i32, [vp, vp, sz]),
         "fa_paged_decode_attn": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_store_attn": (i32, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, sz, vp]),
         "fa_paged_decode_attn_noalloc": (i32, [vp, i32, vp, vp, i32, vp, i32, i32, vp, vp, vp]),
@@ -232,6 +235,15 @@ class Cache:
     def decode_workspace_bytes(self, layer: int, batch: int, max_seq_len: int) -> int:
         return int(_lib.fa_decode_workspace_bytes(self._h, layer, batch, max_seq_len))
 
+    def bind_extend_workspace(self, workspace) -> None:
+        """fa_cache_bind_extend_workspace: let extend and multi-token decode
+        calls split their last wave through `workspace` (a device tensor of at
+        least extend_workspace_bytes() bytes; None unbinds).  The tensor is
+        kept referenced while bound."""
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(_lib.fa_cache_bind_extend_workspace(self._h, _p(workspace), nbytes))
+        self._extend_ws = workspace
+
     def decode(self, layer: int, q, block_table, seq_lens, max_seq_len: int, out, lse=None, workspace=None,
                stream=None) -> None:
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -288,3 +300,9 @@ def workspace(nbytes: int, device="cuda"):
     """A zeroed, 256-byte-aligned decode workspace of at least nbytes
     (torch-allocated; decode calls leave its counters zero for reuse)."""
     return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def extend_workspace_bytes() -> int:
+    """fa_extend_workspace_bytes: the extend split workspace's size on the
+    current device."""
+    return int(_lib.fa_extend_workspace_bytes())

@@ -341,7 +341,8 @@ void fa_cache_destroy(fa_cache* c) {
 
 fa_status fa_cache_set_flags(fa_cache* c, uint32_t flags) {
   if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
-  if (flags & ~static_cast<uint32_t>(FA_FLAG_EARLY_METADATA)) return fail(FA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if (flags & ~static_cast<uint32_t>(FA_FLAG_EARLY_METADATA | FA_FLAG_EXTEND_SPLIT_ALL))
+    return fail(FA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   c->flags = flags;
   return ok();
 }
@@ -690,6 +691,35 @@ fa_status fa_paged_decode_attn_layers(fa_cache* c, int32_t n, const int32_t* lay
   return ok();
 }
 
+// The cache's split workspace for an extend launch (mode 0 without one).
+static void set_split(const fa_cache* c, ExtendArgs& a) {
+  a.split_ws = c->split_ws;
+  a.split_cap = c->split_cap;
+  a.split_mode = !c->split_ws ? 0 : (c->flags & FA_FLAG_EXTEND_SPLIT_ALL) ? 2 : 1;
+}
+
+size_t fa_extend_workspace_bytes(void) { return ext_split_layout(ext_split_cap()).bytes; }
+
+fa_status fa_cache_bind_extend_workspace(fa_cache* c, void* workspace, size_t bytes) {
+  if (!c) return fail(FA_ERR_INVALID_ARG, "cache is NULL");
+  if (!workspace) {
+    c->split_ws = nullptr;
+    c->split_cap = 0;
+    return ok();
+  }
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  int cap = ext_split_cap();
+  while (cap > 0 && ext_split_layout(cap).bytes > bytes) --cap;
+  if (cap < 1)
+    return fail(FA_ERR_WORKSPACE, "extend workspace %zu bytes < %zu needed for one job", bytes,
+                ext_split_layout(1).bytes);
+  const cudaError_t ce = cudaMemset(workspace, 0, ext_split_layout(cap).off_ml);   // the arrival counters
+  if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "clearing the extend workspace: %s", cudaGetErrorString(ce));
+  c->split_ws = workspace;
+  c->split_cap = cap;
+  return ok();
+}
+
 fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const void* k_ext, const void* v_ext,
                                const int32_t* qo_indptr, const int32_t* prefix_lens, const int32_t* block_table,
                                int32_t max_pages_per_seq, int32_t B, int32_t num_tokens, int32_t max_q_len,
@@ -747,6 +777,7 @@ fa_status fa_paged_extend_attn(fa_cache* c, int32_t layer, const void* q, const 
   a.early_metadata = (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0;
   a.sm_scale = L.d.sm_scale;
   a.err = err;
+  set_split(c, a);
   if ((st = encode_q_map(&a.tm_q, q, num_tokens, L.d.num_q_heads, L.d.head_dim, g))) return st;
   if ((st = encode_ext_map(&a.tm_kx, k_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
   if ((st = encode_ext_map(&a.tm_vx, v_ext, num_tokens, L.d.num_kv_heads, L.d.head_dim))) return st;
@@ -809,6 +840,7 @@ fa_status fa_paged_decode_multi_attn(fa_cache* c, int32_t layer, const void* q, 
   a.early_metadata = (c->flags & FA_FLAG_EARLY_METADATA) ? 1 : 0;
   a.sm_scale = L.d.sm_scale;
   a.err = err;
+  set_split(c, a);
   if ((st = encode_q_map(&a.tm_q, q, num_tokens, L.d.num_q_heads, L.d.head_dim, g))) return st;
   a.tm_kx = s->tm_k;   // no chunk rows in this mode: the chunk maps are never used
   a.tm_vx = s->tm_v;

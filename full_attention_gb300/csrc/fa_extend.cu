@@ -48,6 +48,7 @@
 // (magnitude 65520 or more) saturates to +-65504 and sets FA_DEV_ERR_RANGE;
 // stored prefix rows have no such limit.
 // Every wait is bounded; tensor memory is always freed.
+#include <algorithm>
 #include <cfloat>
 
 #include <cuda_fp8.h>
@@ -141,6 +142,17 @@ struct ExtK {
   int B, Hq, Hkv, g, T, kind, window, page_size, tiles_per_page, num_pages, max_pages_per_seq;
   int max_q_len, max_prefix_len, dslices, early_metadata, num_tokens, keys_in_pages;
   float scale_log2;
+  // Jobs (128-row block, KV head and column slice, sequence) are numbered
+  // row block fastest (last block first), gx row blocks and gy (head,
+  // slice) pairs per sequence.  Jobs from split_from on run as two CTAs, each over half of the
+  // job's key tiles; the second of the two to finish merges both (an arrival
+  // counter per split job).  Their partials: ws_o [job][2][8 lane groups][32
+  // float4 columns][32 lanes] fp32, ws_ml [job][2][128 rows] (base, rounded
+  // sum, unrounded sum, 0), ws_cnt [job], zero between launches.
+  int gx, gy, split_from;
+  float4* ws_o;
+  float4* ws_ml;
+  int* ws_cnt;
 };
 
 // The key tiles one CTA walks: prefix tiles (16-aligned starts, from the
@@ -151,15 +163,18 @@ struct ExtK {
 // depend on the order of the tiles.
 struct ExtPlan {
   int nk;                  // keys per tile
-  int b, h, ds, t0, n, P, qo0;
+  int bx, b, h, ds, t0, n, P, qo0;
   int Pk;                  // keys [0, Pk) come from the slab (P, or all keys when keys_in_pages)
   int kmin, kmax;          // visible key positions of the CTA's rows
   int a0, np;              // first prefix tile start, number of prefix tiles
   int c0, nc;              // first chunk tile start (absolute position), number of chunk tiles
   int rot;                 // walk prefix tiles from tile rot, wrapping
-  __device__ int tiles() const { return np + nc; }
-  __device__ bool prefix(int j) const { return j < np; }
+  int j0, nl;              // this CTA's tiles: [j0, j0 + nl) of the walk
+  int ks, s, slot;         // the job's CTAs (1 or 2), this one's index, split-job index
+  __device__ int tiles() const { return nl; }
+  __device__ bool prefix(int j) const { return j + j0 < np; }
   __device__ int start(int j) const {
+    j += j0;
     if (j < np) {
       int k = j + rot;
       if (k >= np) k -= np;
@@ -172,10 +187,26 @@ struct ExtPlan {
 template <int NK>
 __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   x.nk = NK;
-  x.b = blockIdx.z;
-  x.h = blockIdx.y / p.dslices;
-  x.ds = blockIdx.y % p.dslices;
-  x.t0 = blockIdx.x * p.T;
+  const int cta = static_cast<int>(blockIdx.x);
+  int job = cta;
+  x.ks = 1;
+  x.s = 0;
+  x.slot = -1;
+  if (cta >= p.split_from) {
+    job = p.split_from + (cta - p.split_from) / 2;
+    x.s = (cta - p.split_from) & 1;
+    x.ks = 2;
+    x.slot = job - p.split_from;
+  }
+  // row blocks in descending order: a later block of a chunk sees more keys
+  // (causal), so the launch runs the longest jobs first and leaves the
+  // shortest for the last wave
+  x.bx = p.gx - 1 - job % p.gx;
+  const int hy = (job / p.gx) % p.gy;
+  x.b = job / (p.gx * p.gy);
+  x.h = hy / p.dslices;
+  x.ds = hy % p.dslices;
+  x.t0 = x.bx * p.T;
   x.qo0 = __ldg(p.qo_indptr + x.b);
   x.n = __ldg(p.qo_indptr + x.b + 1) - x.qo0;
   bool bad = false;
@@ -195,7 +226,7 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
     if (x.P < 0) { x.P = 0; bad = true; }
     x.Pk = x.P;
   }
-  if (bad && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, FA_DEV_ERR_BOUND);
+  if (bad && threadIdx.x == 0 && x.bx == 0 && job % (p.gx * p.gy) == 0 && x.s == 0) atomicOr(p.err, FA_DEV_ERR_BOUND);
   if (x.t0 >= x.n) return false;
   const int q_first = x.P + x.t0;
   const int q_last = x.P + min(x.t0 + p.T, x.n) - 1;
@@ -207,7 +238,14 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
   const int cfirst = max(x.kmin, x.Pk);
   x.c0 = x.Pk + ((cfirst - x.Pk) / NK) * NK;
   x.nc = (x.kmax >= x.c0) ? (x.kmax - x.c0) / NK + 1 : 0;
-  x.rot = x.np > 1 ? static_cast<int>((blockIdx.x * 2u + x.ds) * 5u % static_cast<unsigned>(x.np)) : 0;
+  x.rot = x.np > 1 ? static_cast<int>((static_cast<unsigned>(x.bx) * 2u + x.ds) * 5u % static_cast<unsigned>(x.np)) : 0;
+  // a split job's two CTAs take the first and second half of the walk; a
+  // job of one tile runs whole on its first CTA
+  const int nt = x.np + x.nc;
+  if (x.ks > nt) x.ks = nt > 1 ? nt : 1;
+  if (x.s >= x.ks) return false;
+  x.j0 = x.s * nt / x.ks;
+  x.nl = (x.s + 1) * nt / x.ks - x.j0;
   return true;
 }
 
@@ -299,7 +337,12 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
   if (!p.early_metadata) griddep_wait();
   griddep_launch_dependents();
   ExtPlan x;
-  if (!ext_plan<64>(p, x)) return;
+  if (!ext_plan<64>(p, x)) {
+    // no work; the grid still ends only after the kernel before it (later
+    // extend launches rely on that order for the split workspace)
+    griddep_wait();
+    return;
+  }
   const int nt = x.tiles();
 
   if (threadIdx.x == 0) {
@@ -997,9 +1040,100 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     fin = named_bar_and(SMX_BAR, SMX_THREADS, fin);
     const float l_tot = fin ? l_run + sm_l[(half ^ 1) * C::M + r] : 0.f;
     const float l_all = fin ? l_lse + sm_l[(2 + (half ^ 1)) * C::M + r] : 0.f;
-    if (!fin) {
-      if (lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
-    } else {
+    if (!fin && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    if (x.ks == 2) {
+      // A split job: leave this CTA's partial (unnormalised O over its tiles,
+      // the exponent base and both sums) in the workspace, then arrive; the
+      // second arrival combines the two on a common base.  Each lane moves
+      // whole 16-byte pieces of its row, laid out so that a warp's 32 lanes
+      // touch 512 consecutive bytes.  A CTA that timed out still arrives, so
+      // the counter is left zero (its error bit says the output is void).
+      // The arrival result is shared through the idle ring, past the sums (a
+      // static shared variable would take the kernel past its shared-memory
+      // budget at head_dim 512).
+      volatile int& sh_last = *reinterpret_cast<volatile int*>(ring + 4 * C::M * sizeof(float));
+      const float base = (m_run > -INFINITY) ? m_run - MB_OFF : -INFINITY;
+      const size_t pj = static_cast<size_t>(x.slot) * 2;
+      const size_t grp = static_cast<size_t>(quarter * 2 + half) * 32;   // this warp's float4 columns
+      if (fin) {
+        float4* po = p.ws_o + (pj + x.s) * (C::M * C::DS / 4) + grp * 32 + lane;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < OH; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + half * OH + c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            po[(c / 4 + e) * 32] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                               __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+        }
+        if (half == 0) p.ws_ml[(pj + x.s) * C::M + r] = make_float4(base, l_tot, l_all, 0.f);
+      }
+      // the barrier orders every lane's partial writes before the release /
+      // acquire add, which publishes them and, for the second arrival, makes
+      // the other CTA's partial visible
+      named_bar_sync(SMX_BAR, SMX_THREADS);
+      if (warp == C::W_MMA + 1 && lane == 0) {
+        const int old = atom_add_acq_rel_gpu(p.ws_cnt + x.slot, 1);
+        int last = 0;
+        if (old == 1) {
+          last = 1;
+          atomicExch(p.ws_cnt + x.slot, 0);   // zero for the next launch
+        } else if (old != 0) {
+          atomicOr(p.err, FA_DEV_ERR_WORKSPACE);
+        }
+        sh_last = last;
+      }
+      named_bar_sync(SMX_BAR, SMX_THREADS);
+      if (sh_last && fin) {
+        // the combination is written in the CTAs' split order (first half of
+        // the tiles, then second), not in arrival order, so the result does
+        // not depend on which CTA finished last
+        const float4 om = __ldcg(p.ws_ml + (pj + (x.s ^ 1)) * C::M + r);
+        const bool first = x.s == 0;
+        const float b0 = first ? base : om.x, b1 = first ? om.x : base;
+        const float bm = fmaxf(b0, b1);
+        const float f0 = (b0 > -INFINITY) ? ex2(b0 - bm) : 0.f;
+        const float f1 = (b1 > -INFINITY) ? ex2(b1 - bm) : 0.f;
+        const float lt = (first ? l_tot : om.y) * f0 + (first ? om.y : l_tot) * f1;
+        const float la = (first ? l_all : om.z) * f0 + (first ? om.z : l_all) * f1;
+        const float inv = (lt > 0.f) ? 1.0f / lt : 0.f;
+        const float w0 = f0 * inv, w1 = f1 * inv;
+        const float4* oo = p.ws_o + (pj + (x.s ^ 1)) * (C::M * C::DS / 4) + grp * 32 + lane;
+        __nv_bfloat16* orow =
+            p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS + half * OH;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < OH; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + half * OH + c, o);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float4 v = __ldcg(oo + (c / 4 + e) * 32);
+              const float oth[4] = {v.x, v.y, v.z, v.w};
+              float y[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float own = __uint_as_float(o[4 * e + k]);
+                y[k] = (first ? own : oth[k]) * w0 + (first ? oth[k] : own) * w1;
+              }
+              w[2 * e] = pack_bf16x2(y[0], y[1]);
+              w[2 * e + 1] = pack_bf16x2(y[2], y[3]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              reinterpret_cast<uint4*>(orow + c)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+        if (row_ok && half == 0 && x.ds == 0 && p.lse)
+          p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
+              (bm > -INFINITY && la > 0.f) ? (bm + __log2f(la)) * 0.69314718055994531f : -INFINITY;
+      }
+    } else if (fin) {
       tc_fence_after();
       const float inv = (l_tot > 0.f) ? 1.0f / l_tot : 0.f;
       __nv_bfloat16* orow =
@@ -1040,9 +1174,28 @@ static cudaError_t launch_extend_t(const ExtendArgs& a, const ExtK& k, cudaStrea
   static unsigned int done = 0;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(extend_kernel<D, KV>), C::SMEM_ALLOC, &done);
   if (e != cudaSuccess) return e;
-  const dim3 grid((a.max_q_len + k.T - 1) / k.T, a.Hkv * k.dslices, a.B);
-  return launch_pdl(extend_kernel<D, KV>, grid, dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q, *a.tm_k, *a.tm_v, a.tm_kx,
-                    a.tm_vx, k);
+  const long long jobs = static_cast<long long>(k.gx) * k.gy * a.B;
+  const long long ctas = k.split_from + 2 * (jobs - k.split_from);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_pdl(extend_kernel<D, KV>, dim3(static_cast<unsigned>(ctas)), dim3(C::NTHR), C::SMEM_ALLOC, s, a.tm_q,
+                    *a.tm_k, *a.tm_v, a.tm_kx, a.tm_vx, k);
+}
+
+// The jobs (from the end of the launch order) that run as two CTAs each.
+// One CTA fits an SM, so a launch of J equal jobs takes ceil(J / SMs) job
+// times; when its last wave is at most half full, splitting that wave's jobs
+// in two (so every SM has at most half a job left) saves up to half a job
+// time, less the partials' write and merge, which long jobs (8 key tiles or
+// more, estimated from the length bounds) amortise.
+static int split_jobs(const ExtendArgs& a, long long jobs) {
+  if (!a.split_ws || a.split_mode == 0 || jobs <= 0) return 0;
+  if (a.split_mode == 2) return static_cast<int>(jobs < a.split_cap ? jobs : a.split_cap);
+  const long long sms = sm_count();
+  const long long tail = jobs % sms;
+  const long long keys = (a.kind == FA_SLIDING ? std::min(a.max_prefix_len, a.window) : a.max_prefix_len) +
+                         a.max_q_len / 2;
+  if (tail == 0 || 2 * tail > sms || keys < 8 * 64 || tail > a.split_cap) return 0;
+  return static_cast<int>(tail);
 }
 
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
@@ -1079,6 +1232,19 @@ cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s) {
   k.dslices = a.D / ExtCfg<256>::DS;
   k.early_metadata = a.early_metadata;
   k.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  k.gx = (a.max_q_len + k.T - 1) / k.T;
+  k.gy = a.Hkv * k.dslices;
+  const long long jobs = static_cast<long long>(k.gx) * k.gy * a.B;
+  if (jobs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int nsplit = split_jobs(a, jobs);
+  k.split_from = static_cast<int>(jobs - nsplit);
+  if (nsplit > 0) {
+    const ExtSplitLayout l = ext_split_layout(a.split_cap);
+    uint8_t* ws = static_cast<uint8_t*>(a.split_ws);
+    k.ws_cnt = reinterpret_cast<int*>(ws);
+    k.ws_ml = reinterpret_cast<float4*>(ws + l.off_ml);
+    k.ws_o = reinterpret_cast<float4*>(ws + l.off_o);
+  }
   if (a.kv_dtype == FA_KV_INT8)
     return a.D == 256 ? launch_extend_t<256, FA_KV_INT8>(a, k, s) : launch_extend_t<512, FA_KV_INT8>(a, k, s);
   if (a.kv_dtype == FA_KV_FP8)

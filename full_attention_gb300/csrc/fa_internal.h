@@ -53,6 +53,8 @@ struct fa_cache {
   int32_t kv_dtype = FA_KV_BF16;
   uint32_t flags = 0;   // FA_FLAG_*
   int32_t err_slot = -1;   // this cache's device error word (index into the per-device array)
+  void* split_ws = nullptr;   // extend split workspace (caller's memory), split_cap jobs
+  int32_t split_cap = 0;
 };
 
 namespace fa {
@@ -180,7 +182,33 @@ struct ExtendArgs {
   // per-call maps: q as (64-column block, head, token, block index) boxes of
   // (64, g, 128/g, 1); k_ext / v_ext as (64, block, KV head, token) boxes of (64, 1, 1, 64)
   CUtensorMap tm_q, tm_kx, tm_vx;
+  // the cache's split workspace (null: none), the jobs it holds, and the
+  // mode: 0 no split, 1 the last wave's jobs when that wave is at most half
+  // full and the jobs are long, 2 the last split_cap jobs whatever their size
+  void* split_ws;
+  int split_cap, split_mode;
 };
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t s);
+
+// Split workspace of extend for `cap` jobs: arrival counters, then per job
+// and CTA 128 rows of (base, rounded sum, unrounded sum, 0), then per job
+// and CTA a 128 x 256 fp32 partial O; each part 256-byte aligned.
+struct ExtSplitLayout {
+  size_t off_ml, off_o, bytes;
+};
+inline ExtSplitLayout ext_split_layout(int cap) {
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  ExtSplitLayout l;
+  l.off_ml = up(static_cast<size_t>(cap) * sizeof(int));
+  l.off_o = l.off_ml + up(static_cast<size_t>(cap) * 2 * 128 * 16);
+  l.bytes = l.off_o + static_cast<size_t>(cap) * 2 * 128 * 256 * sizeof(float);
+  return l;
+}
+// Jobs the split workspace of this device holds: half the SMs (the largest
+// last wave worth splitting in two).
+inline int ext_split_cap() {
+  const int n = sm_count() / 2;
+  return n > 0 ? n : 1;
+}
 
 }  // namespace fa

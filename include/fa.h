@@ -101,7 +101,8 @@ typedef enum { FA_FULL = 0, FA_SLIDING = 1 } fa_layer_kind;
 #define FA_DEV_ERR_SLOT 0x2u       /* a store slot was >= num_pages * page_size    */
 #define FA_DEV_ERR_BOUND 0x4u      /* a length exceeded the caller's max bound      */
 #define FA_DEV_ERR_TIMEOUT 0x8u    /* a bounded barrier wait ran out                */
-#define FA_DEV_ERR_WORKSPACE 0x10u /* decode workspace counters were not zero      */
+#define FA_DEV_ERR_WORKSPACE 0x10u /* decode or extend-split workspace counters
+                                      were not zero                                 */
 #define FA_DEV_ERR_RANGE 0x20u     /* a value out of the kernels' range: an f16
                                       operand saturated (8-bit formats: a q, or
                                       an extend k_ext / v_ext, magnitude of 65520
@@ -150,6 +151,7 @@ FA_API void fa_cache_destroy(fa_cache* cache);
 
 /* Cache flags (fa_cache_set_flags). */
 #define FA_FLAG_EARLY_METADATA 0x1u
+#define FA_FLAG_EXTEND_SPLIT_ALL 0x2u
 
 /* Set FA_FLAG_* options for every later call on this cache (default 0).
  * FA_FLAG_EARLY_METADATA: the caller guarantees that the index arrays of each
@@ -159,10 +161,39 @@ FA_API void fa_cache_destroy(fa_cache* cache);
  * copied from the host).  The kernels, which launch with programmatic
  * dependent launch, then read them while that kernel is still finishing, and
  * wait for it only before touching q, k, v, the slabs and the outputs.
- * Without the flag every read waits.  Unknown bits: FA_ERR_INVALID_ARG.
- * No counterpart on the pages: this is a launch-latency option of this
- * library.  Host only. */
+ * Without the flag every read waits.
+ * FA_FLAG_EXTEND_SPLIT_ALL: with an extend workspace bound
+ * (fa_cache_bind_extend_workspace), split as many jobs of every extend and
+ * multi-token decode launch as it holds, whatever their size (the merge is
+ * then exercised on any input; slower in general).
+ * Unknown bits: FA_ERR_INVALID_ARG.  No counterpart on the pages: these are
+ * launch options of this library.  Host only. */
 FA_API fa_status fa_cache_set_flags(fa_cache* cache, uint32_t flags);
+
+/* Bytes of the extend split workspace on the current device (about 20 MB on
+ * 152 SMs).  The extend kernel runs one CTA per SM, one per job (a 128-row
+ * block of one sequence's queries, one KV head, one 256-column output
+ * slice), all jobs of a launch about equally long on uniform inputs; when a
+ * launch's last wave would leave more than half of the SMs idle, the jobs of
+ * that wave can each run as two CTAs over the two halves of their key tiles,
+ * merged on a common softmax base by the second to finish.  The workspace
+ * holds those jobs' partials (half the SM count of jobs).  No counterpart on
+ * the pages: a scheduling option of this library.  Host only. */
+FA_API size_t fa_extend_workspace_bytes(void);
+
+/* Let extend (fa_paged_extend_attn) and multi-token decode
+ * (fa_paged_decode_multi_attn) calls on `cache` split their last wave as
+ * described above, through `workspace`: device memory of the current device,
+ * 256-byte aligned, of `bytes` >= the partials of one job (fewer than
+ * fa_extend_workspace_bytes() bytes holds fewer jobs).  The caller keeps
+ * ownership; it must stay allocated while calls may use it, and calls on
+ * the cache that use it must run in stream order (one stream, or streams
+ * ordered by events): concurrent calls would share its slots.  Zeroes its
+ * arrival counters (synchronous); each launch leaves them zero.  A launch
+ * splits when the wave is at most half full and its length bounds promise
+ * 8 key tiles (512 keys) or more per job.  NULL unbinds.  Errors: FA_ERR_INVALID_ARG
+ * (misaligned), FA_ERR_WORKSPACE (too small for one job), FA_ERR_CUDA. */
+FA_API fa_status fa_cache_bind_extend_workspace(fa_cache* cache, void* workspace, size_t bytes);
 
 /* Give the sliding layers' slabs a page pool of their own (the pages' window
  * pool: "FreeToken PR #898", description, the window slots come from one

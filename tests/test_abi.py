@@ -151,6 +151,29 @@ def test_cache_flags(fa):
     assert e.value.status == fa.ERR_INVALID_ARG
 
 
+def test_extend_split_workspace_binding(fa):
+    """The extend split workspace: its size follows the layout (arrival
+    counters, per job and CTA 128 rows of 16 bytes and a 128 x 256 fp32
+    partial, each part 256-byte aligned) for half the SMs' jobs; binding
+    refuses a misaligned or too small buffer before any CUDA call; NULL
+    unbinds; the split-every-job flag is accepted."""
+    lib = ctypes.CDLL(fa.LIB_PATH)
+    lib.fa_extend_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_cache_bind_extend_workspace.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
+    up = lambda b: (b + 255) // 256 * 256
+    one = up(4) + up(2 * 128 * 16) + 2 * 128 * 256 * 4
+    total = fa.extend_workspace_bytes()
+    caps = [n for n in range(1, 2048) if up(4 * n) + up(n * 2 * 128 * 16) + n * 2 * 128 * 256 * 4 == total]
+    assert len(caps) == 1 and caps[0] >= 1          # half the SM count (152 SMs: 76 jobs, about 20 MB)
+    c = fa.Cache([lay(FULL, 512, 8, 1)], 8, 16)
+    assert lib.fa_cache_bind_extend_workspace(c._h, 0x1000 + 16, total) == fa.ERR_INVALID_ARG
+    assert lib.fa_cache_bind_extend_workspace(c._h, 0x1000, one - 1) == fa.ERR_WORKSPACE
+    assert lib.fa_cache_bind_extend_workspace(c._h, None, 0) == fa.OK
+    assert lib.fa_cache_bind_extend_workspace(None, None, 0) == fa.ERR_INVALID_ARG
+    c.set_flags(fa.FLAG_EARLY_METADATA | fa.FLAG_EXTEND_SPLIT_ALL)
+    c.set_flags(0)
+
+
 def test_8bit_formats_reach_extend_and_multi_token_decode(fa):
     """Extend and multi-token decode serve the 8-bit formats: with no slab
     bound the calls stop at that check (before any pointer is read or any

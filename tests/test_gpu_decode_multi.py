@@ -66,6 +66,19 @@ def test_multi_token_decode(spec):
     assert c.fa.device_error() == 0
 
 
+@pytest.mark.parametrize("spec", CASES[:3], ids=["F512_g8", "S256_g8_W64", "S256_g2_W1024"])
+def test_multi_token_decode_split(spec):
+    """Every job split over two CTAs and merged through the workspace."""
+    layer, prefix, new = spec
+    c = ExtendCase([layer], prefix, new, seed=12, poison_tail=False, split="all")
+    _store_chunk(c, 0)
+    out, lse = _decode_multi(c, 0)
+    assert_close(out, c.oracle(0), what="split multi-token decode")
+    g = lse.double().cpu().numpy()
+    assert np.all(np.abs(g - c.oracle_lse) <= 2e-3 * np.maximum(1.0, np.abs(c.oracle_lse)))
+    assert c.fa.device_error() == 0
+
+
 def test_one_new_token_equals_decode():
     """n_b = 1 for every sequence: the same attention as the single-token decode."""
     layer = lay(W.SLIDING, 256, 8, 1, 48)

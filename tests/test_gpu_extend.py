@@ -22,7 +22,7 @@ class ExtendCase:
     """One extend call per layer over a paged prefix plus a chunk."""
 
     def __init__(self, layers, prefix, chunk, seed=0, page_size=16, device="cuda", poison_tail=True,
-                 early_metadata=False, poison_window=True):
+                 early_metadata=False, poison_window=True, split=None):
         import full_attention_gb300 as fa
         self.fa = fa
         self.layers = layers
@@ -36,8 +36,15 @@ class ExtendCase:
         plan = W.plan_pages(np.maximum(total, 1), page_size, seed)
         self.bt_np = plan.block_table
         self.cache = fa.Cache(layers, plan.num_pages, page_size)
-        if early_metadata:
-            self.cache.set_flags(fa.FLAG_EARLY_METADATA)
+        flags = (fa.FLAG_EARLY_METADATA if early_metadata else 0) | (fa.FLAG_EXTEND_SPLIT_ALL if split == "all" else 0)
+        if flags:
+            self.cache.set_flags(flags)
+        self.ws = None
+        if split is not None:
+            # the split workspace: "tail" splits as the bench launches do
+            # (the last wave's jobs when worth it), "all" every job it holds
+            self.ws = fa.workspace(fa.extend_workspace_bytes(), device)
+            self.cache.bind_extend_workspace(self.ws)
         self.src = [self.cache.source(i) for i in range(len(layers))]
         self.slabs = self.cache.allocate(device)
         for i, (k, v, _, _) in self.slabs.items():
@@ -147,6 +154,26 @@ def test_small_extend(spec):
     assert c.fa.device_error() == 0
 
 
+@pytest.mark.parametrize("spec", SMALL, ids=[f"{'F' if s[0]['kind'] == 0 else 'S'}{s[0]['head_dim']}"
+                                             f"_g{s[0]['num_q_heads'] // s[0]['num_kv_heads']}_W{s[0]['window']}"
+                                             for s in SMALL])
+def test_small_extend_split(spec):
+    """Every job split over two CTAs (the first and second half of its key
+    tiles) and merged through the workspace: the same parity with the
+    oracle, and the workspace's arrival counters are zero afterwards."""
+    layer, prefix, chunk = spec
+    c = ExtendCase([layer], prefix, chunk, seed=7, split="all")
+    out = c.run(0)
+    assert_close(out, c.oracle(0), what="split extend")
+    g = c.lse[: c.N].double().cpu().numpy()
+    assert np.all(np.abs(g - c.oracle_lse) <= 2e-3 * np.maximum(1.0, np.abs(c.oracle_lse)))
+    assert c.fa.device_error() == 0
+    cap = (torch.cuda.get_device_properties(0).multi_processor_count // 2) or 1
+    assert int(c.ws[: 4 * cap].view(torch.int32).abs().sum()) == 0
+    # a second call over the same workspace gives the same output
+    assert torch.equal(c.run(0), out)
+
+
 def test_shared_layer_extend_reads_source_slab_and_chunk():
     layers = [lay(W.SLIDING, 256, 8, 2, 64), lay(W.FULL, 512, 8, 1), lay(W.SLIDING, 256, 8, 2, 64, W.KV_AUTO)]
     c = ExtendCase(layers, [50, 130], [70, 20], seed=8)
@@ -174,15 +201,18 @@ def test_extend_equals_decode_at_the_last_position_and_early_metadata():
     assert_close(dout[0], out[39].double().cpu().numpy(), atol=1e-2, rel=2e-2, what="decode vs extend")
 
 
-def test_chunked_prefill_workload():
+@pytest.mark.parametrize("split", [None, "tail"])
+def test_chunked_prefill_workload(split):
     """The chunked-prefill workload: 4 prompts of 4096 tokens in 512-token
-    chunks.  Chunks 0, 3 and 7 of both layers are compared on sampled rows."""
+    chunks.  Chunks 0, 3 and 7 of both layers are compared on sampled rows,
+    without and with the split workspace the bench binds (its head_dim-512
+    launches of 512 jobs then split their last wave on a 152-SM device)."""
     w = W.chunked_prefill()
     B, S, Cn = w.batch, w.prompt_len, w.chunk
     rng = np.random.default_rng(2)
     for ci in (0, 3, 7):
         P = ci * Cn
-        c = ExtendCase(w.layers, [P] * B, [Cn] * B, seed=20 + ci)
+        c = ExtendCase(w.layers, [P] * B, [Cn] * B, seed=20 + ci, split=split)
         for li in range(2):
             out = c.run(li)
             d = w.layers[li]

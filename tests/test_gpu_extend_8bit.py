@@ -34,7 +34,7 @@ class Case8:
     rows before they are stored."""
 
     def __init__(self, layers, prefix, chunk, kv_dtype, seed, page_size=16, store_chunk=False, mag=1.0,
-                 poke=None):
+                 poke=None, split=None):
         import full_attention_gb300 as fa
         self.fa, self.layers, self.kv, self.ps = fa, layers, kv_dtype, page_size
         self.prefix = np.asarray(prefix, np.int32)
@@ -44,6 +44,12 @@ class Case8:
         plan = W.plan_pages(np.maximum(total, 1), page_size, seed)
         self.bt_np = plan.block_table
         self.cache = fa.Cache(layers, plan.num_pages, page_size, kv_dtype)
+        if split is not None:
+            # "tail": split as the bench launches do; "all": every job the workspace holds
+            if split == "all":
+                self.cache.set_flags(fa.FLAG_EXTEND_SPLIT_ALL)
+            self.ws = fa.workspace(fa.extend_workspace_bytes(), "cuda")
+            self.cache.bind_extend_workspace(self.ws)
         self.src = [self.cache.source(i) for i in range(len(layers))]
         self.slabs = self.cache.allocate("cuda")
         self.indptr = np.concatenate([[0], np.cumsum(self.chunk)]).astype(np.int32)
@@ -166,6 +172,19 @@ def test_8bit_extend(spec, kv_dtype):
 
 
 @pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
+@pytest.mark.parametrize("spec", EXTEND, ids=[f"{'F' if s[0]['kind'] == 0 else 'S'}{s[0]['head_dim']}"
+                                              f"_g{s[0]['num_q_heads'] // s[0]['num_kv_heads']}_W{s[0]['window']}"
+                                              for s in EXTEND])
+def test_8bit_extend_split(spec, kv_dtype):
+    """Every job split over two CTAs and merged through the workspace (the
+    8-bit exponent base, 2^7 below the running maximum, joins the merge)."""
+    layer, prefix, chunk = spec
+    c = Case8([layer], prefix, chunk, kv_dtype, seed=31, split="all")
+    _check(c.extend(0), c.oracle_extend(0), "8-bit split extend")
+    assert c.fa.device_error() == 0
+
+
+@pytest.mark.parametrize("kv_dtype", FORMATS, ids=IDS)
 def test_8bit_extend_shared_layer(kv_dtype):
     layers = [lay(W.SLIDING, 256, 8, 2, 64), lay(W.FULL, 512, 8, 1), lay(W.SLIDING, 256, 8, 2, 64, W.KV_AUTO)]
     c = Case8(layers, [50, 130], [70, 20], kv_dtype, seed=32)
@@ -216,13 +235,14 @@ def test_8bit_chunked_prefill_workload(kv_dtype):
     chunks, sliding D 256 W 1024 with 16 q / 8 KV heads and full D 512 with
     16 q / 2 KV heads) over 8-bit slabs, at full size: chunks 0, 3 and 7 of
     both layers, on sampled rows that include the first and last rows and the
-    boundary between the first two sequences, every query head of each."""
+    boundary between the first two sequences, every query head of each.  The
+    split workspace is bound as in the bench."""
     w = W.chunked_prefill()
     B, Cn = w.batch, w.chunk
     rng = np.random.default_rng(5)
     for ci in (0, 3, 7):
         P = ci * Cn
-        c = Case8(w.layers, [P] * B, [Cn] * B, kv_dtype, seed=40 + ci)
+        c = Case8(w.layers, [P] * B, [Cn] * B, kv_dtype, seed=40 + ci, split="tail")
         for li in range(len(w.layers)):
             out, lse = c.extend(li)
             d = w.layers[li]
