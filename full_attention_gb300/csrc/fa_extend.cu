@@ -114,7 +114,14 @@ struct ExtCfg {
   static constexpr uint32_t Q_COL0 = DS + 128;
   static_assert(Q_COL0 + NQT * 32 == TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-  static_assert((1 + 3 * NSLOT + 2 + 2 + 2 + 1 + 1 + 1 + 2 * SCL_R) * 8 <= BAR_BYTES, "barrier space");
+  static_assert((1 + 3 * NSLOT + 2 + 2 + 2 + 1 + 1 + 1 + 2 * SCL_R + 2) * 8 <= BAR_BYTES, "barrier space");
+  // Q's tensor-memory blocks arrive by TMA into the ring's last QST slots
+  // (the boxes' 128-byte-swizzled layout, 16 KB per block) and the softmax
+  // warps move them into tensor memory; the producers' first fill of those
+  // slots waits until they have
+  static constexpr int QST = NQT * (M * 128) / SLOT;
+  static constexpr int QST_OFF = (NSLOT - QST) * SLOT;
+  static_assert(NQT * (M * 128) % SLOT == 0 && QST >= 1 && QST < NSLOT, "Q staging slots");
   static_assert(NSLOT >= KB / CPS + NVB / CPS, "a ring must hold one tile");
   // a producer warp's consecutive slots lie NPW ring positions apart; its
   // parity wait on a slot's empty barrier is sound only while that is at most
@@ -309,6 +316,18 @@ __device__ __forceinline__ short max_code(float m, bool& out_of_range) {
 }
 __device__ __forceinline__ float max_decode(short c) { return c == -32768 ? -INFINITY : static_cast<float>(c); }
 
+// One bulk copy from shared to global memory (both addresses 16-byte
+// aligned, size a multiple of 16), tracked by this thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+// Wait until every bulk copy this thread issued has read its shared-memory source.
+__device__ __forceinline__ void bulk_store_drain() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 template <int D, int KV>
 __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -331,6 +350,8 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
   uint64_t* sc_full = qt_full + 3;      // 8-bit slabs: [SCL_R] a tile's scales are written
   uint64_t* sc_empty = sc_full + C::SCL_R;   // [SCL_R] the softmax has read them
   uint64_t* land = sc_empty + C::SCL_R;      // 8-bit slabs: [NSLOT] a slot's TMA data has landed
+  uint64_t* qst_full = land + C::NSLOT;      // Q's tensor-memory blocks have landed in the staging slots
+  uint64_t* q_free = qst_full + 1;           // the softmax warps have read them: the slots may be filled
   float* scl = reinterpret_cast<float*>(smem + C::OFF_SCL);   // [SCL_R][3][64]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -361,6 +382,8 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     mbar_init(&o_bar[1], 1);
     mbar_init(qt_full, C::NSMX);
     mbar_init(&done_bar, 1);
+    mbar_init(qst_full, 1);
+    mbar_init(q_free, C::NSMX);
     if constexpr (C::Q8) {
       for (int i = 0; i < C::SCL_R; ++i) {
         mbar_init(&sc_full[i], 32);        // the 32 lanes of producer warp 0
@@ -394,14 +417,16 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     const int pw = warp < C::NPW ? warp : C::NPW;   // NPW: the 8-bit loader warp
     const uint64_t pol = l2_policy_evict_last();   // K/V rows are shared by the CTAs of a (sequence, head)
     if (threadIdx.x == 0) {
-      if constexpr (KV == FA_KV_BF16) {
-        prefetch_tmap(&tm_q);
-        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-        for (int kb = C::NQT; kb < C::KB; ++kb)
-          tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
-      } else {
-        mbar_arrive_expect_tx(q_full, 0);   // the softmax warps write Q, as f16, themselves
-      }
+      // Q (bf16, both formats): its tensor-memory blocks into the staging
+      // slots, the rest into its shared-memory blocks (8-bit slabs: the
+      // softmax warps then rewrite those in place as f16)
+      prefetch_tmap(&tm_q);
+      mbar_arrive_expect_tx(qst_full, C::NQT * (C::M * 128));
+      for (int kb = 0; kb < C::NQT; ++kb)
+        tma_load_4d(ring + C::QST_OFF + kb * (C::M * 128), &tm_q, qst_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int kb = C::NQT; kb < C::KB; ++kb)
+        tma_load_4d(qs + (kb - C::NQT) * (C::M * 128), &tm_q, q_full, 0, x.h * p.g, x.qo0 + x.t0, kb, pol);
     }
     if (lane == 0) {
       prefetch_tmap(&tm_k);
@@ -538,7 +563,10 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
         const int sl = e % C::NSLOT;
         if (pw == C::NPW) {
           bool w = true;
-          if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+          if (lane == 0) {
+            w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+            if (e < C::NSLOT && e >= C::NSLOT - C::QST) w = mbar_wait(q_free, 0) && w;   // Q's staging slots
+          }
           ok = __shfl_sync(0xffffffffu, w, 0) && ok;
           if (ok) {
             uint8_t* dst = ring + sl * C::SLOT;
@@ -589,7 +617,10 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
       if (e % C::NPW == pw) {
         const int sl = e % C::NSLOT;
         bool w = true;
-        if (lane == 0) w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+        if (lane == 0) {
+          w = mbar_wait(&empty[sl], ((e / C::NSLOT) & 1) ^ 1);
+          if (e < C::NSLOT && e >= C::NSLOT - C::QST) w = mbar_wait(q_free, 0) && w;   // Q's staging slots
+        }
         ok = __shfl_sync(0xffffffffu, w, 0) && ok;
         if (ok) {
           uint8_t* dst = ring + sl * C::SLOT;
@@ -724,7 +755,7 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
             !mbar_wait(C::Q8 ? &land[i % C::NSLOT] : &full[i % C::NSLOT], (i / C::NSLOT) & 1))
           atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
     }
-    if (threadIdx.x == 0 && !mbar_wait(q_full, 0)) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    if (threadIdx.x == 0 && !(mbar_wait(q_full, 0) && mbar_wait(qst_full, 0))) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
   } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------- MMA issuer
     // The whole warp walks the schedule and waits on the barriers, so slot
@@ -839,28 +870,29 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     {
       // this row's first NQT * 64 query values into tensor memory (row =
-      // lane, bf16 pairs per column: the A-operand layout of the S MMA),
-      // half h copying blocks h, h + 2, ...; rows past the last token are zero.
-      // For 8-bit slabs the MMAs run in f16: every block of the row goes as
-      // f16, the rest of Q into its shared-memory blocks (the layout the TMA
-      // boxes would give)
-      const int tok = x.qo0 + t;
-      const bool in = tok < p.num_tokens;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(in ? tok : 0) * p.Hq + x.h * p.g + hj) * D);
-      constexpr int QBLK = KV == FA_KV_BF16 ? C::NQT : C::KB;
+      // lane, 16-bit pairs per column: the A-operand layout of the S MMA),
+      // half h moving blocks h, h + 2, ... out of the staging slots (rows past
+      // the last token arrive as zeros).  8-bit slabs: the MMAs run in f16,
+      // so those values go as f16, and Q's shared-memory blocks are rewritten
+      // in place as f16 too.  Then the staging slots are released.
+      bool qok = mbar_wait(qst_full, 0);
+      if constexpr (C::Q8) qok = mbar_wait(q_full, 0) && qok;
+      if (!__all_sync(0xffffffffu, qok) && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+      constexpr int QBLK = C::Q8 ? C::KB : C::NQT;
       uint32_t qbig = 0;
 #pragma unroll 1
       for (int kb = half; kb < QBLK; kb += 2) {
+        uint8_t* blk = kb < C::NQT ? ring + C::QST_OFF + kb * (C::M * 128) : qs + (kb - C::NQT) * (C::M * 128);
         uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = in ? __ldg(src + kb * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(blk + sw128(r, u));
+          w[4 * u] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
         }
-        if constexpr (KV != FA_KV_BF16) {
+        if constexpr (C::Q8) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             qbig |= bf16x2_past_f16(w[i]);
@@ -869,21 +901,23 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
         }
         if (kb < C::NQT) {
           tmem_st32(trow + C::Q_COL0 + kb * 32, w);
-        } else {
-          uint8_t* qb = qs + (kb - C::NQT) * (C::M * 128);
+        } else {   // 8-bit slabs only
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(qb + sw128(r, u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            *reinterpret_cast<uint4*>(blk + sw128(r, u)) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      if constexpr (KV != FA_KV_BF16) {
+      if constexpr (C::Q8) {
         fence_proxy_async_smem();   // the Q rows written here, for the S MMA
         if (__any_sync(0xffffffffu, qbig != 0) && lane == 0) atomicOr(p.err, FA_DEV_ERR_RANGE);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(qt_full);
+      if (lane == 0) {
+        mbar_arrive(qt_full);
+        mbar_arrive(q_free);
+      }
     }
     const int klo = (p.kind == FA_FULL) ? 0 : qpos - p.window + 1;
     const float sc = p.scale_log2;
@@ -1041,6 +1075,24 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     const float l_tot = fin ? l_run + sm_l[(half ^ 1) * C::M + r] : 0.f;
     const float l_all = fin ? l_lse + sm_l[(2 + (half ^ 1)) * C::M + r] : 0.f;
     if (!fin && lane == 0) atomicOr(p.err, FA_DEV_ERR_TIMEOUT);
+    // The output rows leave through the idle ring: each lane puts its row's
+    // 128 bf16 columns (256 bytes; rows 272 bytes apart, so the 16-byte
+    // stores are free of bank conflicts) into its warp's part, then copies
+    // the row out with one bulk copy (plain stores left the SM at about 16
+    // bytes per cycle, ~2 us per CTA).
+    auto stage = [&](int c, const uint32_t (&w)[16]) {   // columns [c, c + 32) of this half
+      uint8_t* stg = ring + 4096 + (quarter * 2 + half) * (32 * 272) + lane * 272;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        *reinterpret_cast<uint4*>(stg + ((c >> 5) * 4 + e) * 16) = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    };
+    auto write_rows = [&]() {
+      const uint8_t* stg = ring + 4096 + (quarter * 2 + half) * (32 * 272) + lane * 272;
+      fence_proxy_async_smem();   // the rows just written, for the bulk copy's reads
+      if (row_ok) bulk_store(p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS + half * OH,
+                             stg, OH * 2);
+      bulk_store_drain();
+    };
     if (x.ks == 2) {
       // A split job: leave this CTA's partial (unnormalised O over its tiles,
       // the exponent base and both sums) in the workspace, then arrive; the
@@ -1101,34 +1153,29 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
         const float inv = (lt > 0.f) ? 1.0f / lt : 0.f;
         const float w0 = f0 * inv, w1 = f1 * inv;
         const float4* oo = p.ws_o + (pj + (x.s ^ 1)) * (C::M * C::DS / 4) + grp * 32 + lane;
-        __nv_bfloat16* orow =
-            p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS + half * OH;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < OH; c += 32) {
           uint32_t o[32];
           tmem_ld32(trow + half * OH + c, o);
           tmem_ld_wait();
-          if (row_ok) {
-            uint32_t w[16];
+          uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float4 v = __ldcg(oo + (c / 4 + e) * 32);
-              const float oth[4] = {v.x, v.y, v.z, v.w};
-              float y[4];
+          for (int e = 0; e < 8; ++e) {
+            const float4 v = __ldcg(oo + (c / 4 + e) * 32);
+            const float oth[4] = {v.x, v.y, v.z, v.w};
+            float y[4];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float own = __uint_as_float(o[4 * e + k]);
-                y[k] = (first ? own : oth[k]) * w0 + (first ? oth[k] : own) * w1;
-              }
-              w[2 * e] = pack_bf16x2(y[0], y[1]);
-              w[2 * e + 1] = pack_bf16x2(y[2], y[3]);
+            for (int k = 0; k < 4; ++k) {
+              const float own = __uint_as_float(o[4 * e + k]);
+              y[k] = (first ? own : oth[k]) * w0 + (first ? oth[k] : own) * w1;
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              reinterpret_cast<uint4*>(orow + c)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            w[2 * e] = pack_bf16x2(y[0], y[1]);
+            w[2 * e + 1] = pack_bf16x2(y[2], y[3]);
           }
+          stage(c, w);
         }
+        write_rows();
         if (row_ok && half == 0 && x.ds == 0 && p.lse)
           p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
               (bm > -INFINITY && la > 0.f) ? (bm + __log2f(la)) * 0.69314718055994531f : -INFINITY;
@@ -1136,23 +1183,18 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     } else if (fin) {
       tc_fence_after();
       const float inv = (l_tot > 0.f) ? 1.0f / l_tot : 0.f;
-      __nv_bfloat16* orow =
-          p.out + (static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj) * D + x.ds * C::DS;
 #pragma unroll 1
-      for (int c = half * OH; c < (half + 1) * OH; c += 32) {
+      for (int c = 0; c < OH; c += 32) {
         uint32_t o[32];
-        tmem_ld32(trow + c, o);
+        tmem_ld32(trow + half * OH + c, o);
         tmem_ld_wait();
-        if (row_ok) {
-          uint32_t w[16];
+        uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            reinterpret_cast<uint4*>(orow + c)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-        }
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+        stage(c, w);
       }
+      write_rows();
       if (row_ok && half == 0 && x.ds == 0 && p.lse)
         p.lse[static_cast<size_t>(x.qo0 + t) * p.Hq + x.h * p.g + hj] =
             (m_run > -INFINITY && l_all > 0.f) ? (m_run - MB_OFF + __log2f(l_all)) * 0.69314718055994531f : -INFINITY;
