@@ -365,31 +365,46 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
     return;
   }
   const int nt = x.tiles();
+  // Producers: the first tile's page ids (block-table reads, index data the
+  // dependency does not cover under early metadata, and already ordered after
+  // it otherwise), issued before the set-up below so that the first K copies
+  // can start as soon as the dependency resolves
+  int pid0 = -1, off0 = 0;
+  if ((warp < C::NPW || (C::Q8 && warp == C::W_LOAD)) && lane < 4 && nt > 0 && x.prefix(0)) {
+    const int pos = x.start(0) + 16 * lane;   // a 16-row group lies in one page
+    if (pos < x.Pk) {
+      const int pg = pos / p.page_size;
+      off0 = pos - pg * p.page_size;
+      pid0 = ld_nc_early(p.block_table + static_cast<size_t>(x.b) * p.max_pages_per_seq + pg);
+    }
+  }
 
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < C::NSLOT; ++i) {
+  if (warp == 0) {
+    // the barriers, initialised by the lanes of warp 0 side by side: lane 0
+    // the single ones, lane 1 + i ring slot i's, lane 16 + i scale slot i's
+    static_assert(C::NSLOT <= 15 && C::SCL_R <= 16, "one lane per ring and scale slot");
+    if (lane == 0) {
+      mbar_init(q_full, 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&s_full[i], 1);
+        mbar_init(&p_full[i], C::NSMX);
+      }
+      mbar_init(&o_bar[0], 1);
+      mbar_init(&o_bar[1], 1);
+      mbar_init(qt_full, C::NSMX);
+      mbar_init(&done_bar, 1);
+      mbar_init(qst_full, 1);
+      mbar_init(q_free, C::NSMX);
+    } else if (lane <= C::NSLOT) {
+      const int i = lane - 1;
       // bf16: the filling warp's lane 0 expect_tx + 32 lane arrivals; 8-bit:
       // one arrival per converting warp
       mbar_init(&full[i], C::Q8 ? C::NPW : 33);
       mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], C::NSMX);
-    }
-    mbar_init(&o_bar[0], 1);
-    mbar_init(&o_bar[1], 1);
-    mbar_init(qt_full, C::NSMX);
-    mbar_init(&done_bar, 1);
-    mbar_init(qst_full, 1);
-    mbar_init(q_free, C::NSMX);
-    if constexpr (C::Q8) {
-      for (int i = 0; i < C::SCL_R; ++i) {
-        mbar_init(&sc_full[i], 32);        // the 32 lanes of producer warp 0
-        mbar_init(&sc_empty[i], C::NSMX);  // one arrival per softmax warp
-      }
-      for (int i = 0; i < C::NSLOT; ++i) mbar_init(&land[i], 32);   // the loader warp's 32 lanes
+      if constexpr (C::Q8) mbar_init(&land[i], 32);   // the loader warp's 32 lanes
+    } else if (C::Q8 && lane >= 16 && lane < 16 + C::SCL_R) {
+      mbar_init(&sc_full[lane - 16], 32);        // the 32 lanes of producer warp 0
+      mbar_init(&sc_empty[lane - 16], C::NSMX);  // one arrival per softmax warp
     }
     fence_mbar_init();
   }
@@ -724,7 +739,7 @@ __global__ void __launch_bounds__(ExtCfg<D, KV>::NTHR, 1)
       if (lane < 2) dst[128 + lane] = lane == 0 ? l0 : l1;
       mbar_arrive(&sc_full[s]);
     };
-    PageRef pid_next = load_pid(0);
+    PageRef pid_next{pid0, off0};   // load_pid(0), read above
     TileSrc src_cur{}, src_prev{};
     for (int t = 0; ok && t <= nt; ++t) {
       if (t < nt) {
