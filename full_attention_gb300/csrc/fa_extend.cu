@@ -17,28 +17,37 @@
 // the first 256 columns of Q as bf16 pairs [384, 512), so S = Q K^T reads
 // that part of Q from tensor memory and only the rest (head_dim 512) from
 // shared memory; the freed shared memory deepens the K/V ring.  Roles:
-//   warps 0-3   producers: the shared-memory part of Q once (4-D map,
-//               rows = (token, head)); per 64-key tile the K tile in
-//               64-column chunks and the V tile of this CTA's output slice,
-//               from slab pages or from k_ext / v_ext, slot e by warp e % 4;
+//   warps 0-3   producers: Q once (4-D map, rows = (token, head)), its
+//               shared-memory blocks in place and its tensor-memory blocks
+//               into the ring's last slots for the softmax warps to move;
+//               per 64-key tile the K tile in 64-column chunks and the V
+//               tile of this CTA's output slice, from slab pages or from
+//               k_ext / v_ext, slot e by warp e % 4;
 //   warp 4      MMA issuer (the whole warp walks the schedule, one elected
 //               lane issues): S_j = Q K_j^T (tcgen05.mma, M=128, N=64, fp32
 //               in TMEM, double buffered), then O += P_{j-1} V_{j-1} with P
 //               read from tensor memory and V as an MN-major operand;
 //   warps 5-12  softmax: two warps per row quarter, each thread one query
-//               row and half of each tile's 64 columns; first copy the row's
-//               leading 256 Q values into tensor memory; per tile load S, mask,
-//               online softmax in the log2 domain, write P (bf16) back into the
-//               S buffer; rescale O in TMEM only when the running max grows by
-//               more than 2^8, so rescales are rare; final normalisation and
-//               bf16 store.
+//               row and half of each tile's 64 columns; first move the row's
+//               leading 256 Q values from the staging slots into tensor
+//               memory; per tile load S, mask, online softmax in the log2
+//               domain, write P (bf16) back into the S buffer; rescale O in
+//               TMEM only when the running max grows by more than 2^8, so
+//               rescales are rare; final normalisation, the rows staged in the
+//               idle ring and copied out by bulk copies.
+// Jobs (a 128-row block, a KV head and column slice, a sequence) form a 1-D
+// grid, the longest row blocks first; with a split workspace bound, the jobs
+// of a last wave that would leave more than half of the SMs idle run as two
+// CTAs each over the two halves of their key tiles, merged by the second to
+// finish.
 // 8-bit slabs (int8 or fp8 per-token-head codes): every MMA operand is f16.
 // A loader warp copies each slot as soon as it is free: a prefix slot's raw
 // codes by TMA into the slot's upper half, a chunk slot's bf16 rows by TMA
 // as in the bf16 path.  The four producer warps then rewrite the slot in
 // place as exact f16 values (int8: a byte permute and one subtraction per
 // pair; e4m3: the hardware pair conversion; chunk rows: bf16 to f16), each
-// taking one 16-row group; the softmax warps write Q as f16.  The per-key scales never touch the
+// taking one 16-row group; the softmax warps convert Q to f16 (its
+// shared-memory blocks in place).  The per-key scales never touch the
 // operands: producer warp 0 puts each tile's K scale (times the softmax
 // scale) and V scale into a small ring beside the tiles; the softmax
 // multiplies the fp32 scores by the K scale and folds the V scale into P.
