@@ -242,7 +242,8 @@ __device__ __forceinline__ bool ext_plan(const ExtK& p, ExtPlan& x) {
     if (x.P < 0) { x.P = 0; bad = true; }
     x.Pk = x.P;
   }
-  if (bad && threadIdx.x == 0 && x.bx == 0 && job % (p.gx * p.gy) == 0 && x.s == 0) atomicOr(p.err, FA_DEV_ERR_BOUND);
+  // one report per sequence, from its first job
+  if (bad && threadIdx.x == 0 && job % (p.gx * p.gy) == 0 && x.s == 0) atomicOr(p.err, FA_DEV_ERR_BOUND);
   if (x.t0 >= x.n) return false;
   const int q_first = x.P + x.t0;
   const int q_last = x.P + min(x.t0 + p.T, x.n) - 1;

@@ -174,6 +174,27 @@ def test_small_extend_split(spec):
     assert torch.equal(c.run(0), out)
 
 
+@pytest.mark.parametrize("split", [None, "all"])
+def test_length_past_its_bound_sets_error_bit(split):
+    """A prefix longer than max_prefix_len, or a chunk longer than max_q_len,
+    is cut to the bound and reported with FA_DEV_ERR_BOUND (several row blocks
+    per sequence: g = 2 packs 64 tokens per block)."""
+    layer = lay(W.FULL, 256, 4, 2)
+    c = ExtendCase([layer], [40, 300], [150, 200], seed=10, split=split)
+    d = c.layers[0]
+    out = torch.zeros((c.N, d["num_q_heads"], d["head_dim"]), dtype=torch.bfloat16, device="cuda")
+    assert c.fa.device_error() == 0
+    # prefix 300 against a bound of 256
+    c.cache.extend(0, c.q[0][: c.N], c.kx[0][: c.N], c.vx[0][: c.N], c.indptr_dev, c.prefix_dev, c.bt, 200, 256, out)
+    assert c.fa.device_error() & c.fa.DEV_ERR_BOUND
+    # chunk 200 against a bound of 128 (the launch covers 128 tokens per sequence)
+    c.cache.extend(0, c.q[0][: c.N], c.kx[0][: c.N], c.vx[0][: c.N], c.indptr_dev, c.prefix_dev, c.bt, 128, 300, out)
+    assert c.fa.device_error() & c.fa.DEV_ERR_BOUND
+    # within both bounds: no bit
+    c.cache.extend(0, c.q[0][: c.N], c.kx[0][: c.N], c.vx[0][: c.N], c.indptr_dev, c.prefix_dev, c.bt, 200, 300, out)
+    assert c.fa.device_error() == 0
+
+
 def test_shared_layer_extend_reads_source_slab_and_chunk():
     layers = [lay(W.SLIDING, 256, 8, 2, 64), lay(W.FULL, 512, 8, 1), lay(W.SLIDING, 256, 8, 2, 64, W.KV_AUTO)]
     c = ExtendCase(layers, [50, 130], [70, 20], seed=8)
