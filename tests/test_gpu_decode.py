@@ -155,6 +155,22 @@ def test_bad_page_id_sets_device_error():
     assert case.fa.device_error() == 0
 
 
+def test_length_past_max_seq_len_sets_device_error():
+    """A sequence longer than the call's max_seq_len is cut to it and
+    reported with FA_DEV_ERR_BOUND; within the bound nothing is reported."""
+    layers = [lay(W.FULL, 512, 8, 1), lay(W.SLIDING, 256, 8, 1, 16)]
+    case = DecodeCase(layers, [40, 50], 16, seed=2)
+    assert case.fa.device_error() == 0
+    real = case.max_len
+    for i in range(len(layers)):
+        case.max_len = 45            # the 50-token sequence is past it
+        case.decode(i)
+        assert case.fa.device_error() & case.fa.DEV_ERR_BOUND
+        case.max_len = real
+        case.decode(i)
+        assert case.fa.device_error() == 0
+
+
 # ------------------------------------------------------------------ full size
 def _sample(B, n, seed):
     return sorted(np.random.default_rng(seed).choice(B, size=min(n, B), replace=False).tolist())
