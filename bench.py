@@ -409,6 +409,7 @@ def gpu_arm(args, rank, world):
         "wall_s_timed": round(wall, 3),
     }
     res["multi_layer_step"] = multi_layer_measure(step, args, torch, flush, hbm)
+    res["decode_store"] = decode_store_measure(step, torch)
     # end to end on every rank; the job's bytes over the slowest rank's time
     if world > 1:
         torch.distributed.barrier()
@@ -509,6 +510,75 @@ def decode_subrecord(name, args, dev, flush):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return rec
+
+
+def decode_store_measure(step, torch):
+    """The per-token store of a decode step on its own (fa_kv_store of the B
+    current rows of one owning layer per head_dim; in the timed step these
+    stores are fused into the decode launches).  They are latency-bound, so
+    the figure is microseconds per call: 50 back-to-back calls in a graph,
+    and a single call between two events inside a graph."""
+    out = {}
+    for D in (256, 512):
+        owners = [i for i in sorted(step.slabs) if step.layers[i]["head_dim"] == D]
+        if not owners:
+            continue
+        i = owners[0]
+        k, v, sl = step.new[i]
+        call = lambda: step.cache.store(i, k, v, sl)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        g = None
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                call()
+            torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(50):
+                    call()
+            torch.cuda.synchronize()
+        except Exception as e:
+            print(f"# decode store graph capture failed ({e})", file=sys.stderr)
+            torch.cuda.synchronize()
+            g = None
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        back = None
+        if g is not None:
+            g.replay()
+            torch.cuda.synchronize()
+            e0.record()
+            g.replay()
+            e1.record()
+            e1.synchronize()
+            back = e0.elapsed_time(e1) * 1e3 / 50
+        # one call between two events, all three captured in a graph, so the
+        # interval is the device's (the host's launch latency stays outside)
+        single = []
+        a, b = torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True)
+        try:
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1):
+                a.record()
+                call()
+                b.record()
+            torch.cuda.synchronize()
+            for _ in range(20):
+                g1.replay()
+                torch.cuda.synchronize()
+                single.append(a.elapsed_time(b) * 1e3)
+        except Exception as e:
+            print(f"# decode store single-call graph failed ({e})", file=sys.stderr)
+            torch.cuda.synchronize()
+            single = [float("nan")]
+        nb = store_bytes(step.layers[i], step.B, step.w.kv_dtype)
+        out[f"D{D}"] = {"layer": i, "rows": step.B * step.layers[i]["num_kv_heads"] * 2, "bytes_per_call": nb,
+                        "us_per_call_back_to_back": None if back is None else round(back, 2),
+                        "us_per_call_single_median": round(float(np.median(single)), 2)}
+    return out
 
 
 def multi_layer_measure(step, args, torch, flush, hbm):
