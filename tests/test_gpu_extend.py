@@ -174,6 +174,27 @@ def test_small_extend_split(spec):
     assert torch.equal(c.run(0), out)
 
 
+def test_split_workspace_for_one_job_and_unbinding():
+    """A workspace with room for one job's partials splits only the last job of
+    the launch (the rest run whole); the output still matches the oracle.
+    Unbinding returns to the unsplit kernel, bit for bit the same as a cache
+    that never had a workspace."""
+    layer = lay(W.FULL, 512, 8, 1)
+    c = ExtendCase([layer], [40, 100, 17], [37, 130, 1], seed=11, split="all")
+    one = 256 + 4096 + 2 * 128 * 256 * 4   # counters, 128 rows x 16 B x 2 CTAs, 2 partials of 128 x 256 fp32
+    small = c.fa.workspace(one)
+    c.cache.bind_extend_workspace(small)
+    assert_close(c.run(0), c.oracle(0), what="one split job")
+    assert c.fa.device_error() == 0
+    assert int(small[:4].view(torch.int32).abs().sum()) == 0
+    c.cache.bind_extend_workspace(None)
+    unsplit = c.run(0).clone()
+    plain = ExtendCase([layer], [40, 100, 17], [37, 130, 1], seed=11)
+    assert torch.equal(unsplit, plain.run(0))
+    with pytest.raises(c.fa.FAError):
+        c.cache.bind_extend_workspace(c.fa.workspace(one - 256))   # too small for one job
+
+
 @pytest.mark.parametrize("split", [None, "all"])
 def test_length_past_its_bound_sets_error_bit(split):
     """A prefix longer than max_prefix_len, or a chunk longer than max_q_len,
